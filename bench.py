@@ -1,0 +1,472 @@
+"""Benchmark of the QSA decode / MTP-verify step on GB300.
+
+Default workload: MTP verify at batch 32, 4 verify queries per request,
+contexts 50,000 + 800*t tokens (t uniform in 0..14, seeded), 1 index head of
+128, 16/2 attention heads of 128, paged BF16 KV (pages of 64, seeded random
+page permutation). One step = qsa_decode: FP32 block scores -> top-512
+selection + unfilled block (width 2,051) -> sparse attention, PDL-chained.
+
+Prints one JSON line. `value` is HBM GB/s of algorithmic bytes (compressed
+keys read once per request + K/V of the union of each request's selected
+positions) over the device time of the step; `latency_us` is the step time.
+L2 is flushed (a write larger than L2) before every timed step and the flush
+is outside the timed events.
+
+    python bench.py [--steps K] [--warmup W] [--config {0,1,2,3,4}] [--impl reference]
+"""
+
+import os
+
+# the oracle baseline runs single-threaded (numpy's BLAS included)
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import re  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_sparse_attention_qsa_gb300 import synth  # noqa: E402
+
+METRIC = "QSA step latency (µs) and HBM GB/s, batch 1–32, 50K ctx, 4 verify queries"
+UNIT = "GB/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--ctx", type=int, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-flush", action="store_true", help="warm-L2 numbers (reported as such)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: every rank runs its own independent batch)
+# ---------------------------------------------------------------------------
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+# ---------------------------------------------------------------------------
+
+def kv_row_bytes(spec):
+    return spec.n_kv_heads * spec.head_dim * (1 if spec.kv_dtype == "fp8" else 2)
+
+
+def kc_bytes(spec):
+    return sum(max(1, (max(qp) + 1) // 4) * spec.n_idx_heads * spec.head_dim * 2 for qp in spec.q_pos())
+
+
+def kv_bytes(spec, sel_pos_host):
+    """(union over each request's queries, plain sum) of selected K+V bytes."""
+    union = 0
+    total = 0
+    for r in range(spec.batch):
+        s = sel_pos_host[r]
+        valid = s[s >= 0]
+        total += valid.size
+        union += np.unique(valid).size
+    row = 2 * kv_row_bytes(spec)  # K and V
+    return union * row, total * row
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+_CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_index=0):
+        self.proc = None
+        self.t0 = self.t1 = None
+        cmd = ["nvidia-smi", f"--query-gpu={_CLOCK_FIELDS}", "--format=csv,noheader,nounits", "-lms", "20"]
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            cmd += ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            pass
+        self.cmd = cmd
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.15)
+        except Exception:
+            self.proc = None
+
+    def mark(self, which):
+        if which == "start":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        rows = [ln.split(",") for ln in out.strip().splitlines() if ln.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def build_lib():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    from block_sparse_attention_qsa_gb300 import qsa
+
+    return qsa
+
+
+def make_gpu_state(qsa, spec):
+    g = synth.make_inputs(spec, device="cuda")
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    kc = torch.zeros((spec.batch, spec.max_blocks(), spec.n_idx_heads, spec.head_dim), dtype=torch.bfloat16,
+                     device="cuda")
+    qsa.compress_keys(d, g["idx_keys"], g["q_pos"], kc, ws)
+    del g["idx_keys"]
+    st = {
+        "g": g, "d": d, "ws": ws, "kc": kc,
+        "scores": torch.empty((spec.batch, spec.n_q, spec.max_blocks()), device="cuda"),
+        "sel_blk": torch.empty((spec.batch, spec.n_q, 512), dtype=torch.int32, device="cuda"),
+        "sel_pos": torch.empty((spec.batch, spec.n_q, 2051), dtype=torch.int32, device="cuda"),
+        "out": torch.empty((spec.batch, spec.n_q, spec.n_q_heads, spec.head_dim), dtype=torch.bfloat16,
+                           device="cuda"),
+    }
+    return st
+
+
+def decode_call(qsa, st, inputs=None, out=None):
+    g = st["g"] if inputs is None else inputs
+    qsa.decode(st["d"], g["q_idx"], st["kc"], g["q"], st["g"]["k_cache"], st["g"]["v_cache"], st["g"]["k_scale"],
+               st["g"]["v_scale"], g["page_table"], g["q_pos"], st["out"] if out is None else out, st["ws"])
+
+
+def timed(fn, steps, flush, stream):
+    """Per-step device times (ms) of fn, with the L2 flush outside the events."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        if flush is not None:
+            flush.zero_()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def ncu_traffic(kernel_tag):
+    """Per-launch DRAM bytes from the committed ncu summary of `kernel_tag`, or
+    None if absent or if the kernel source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
+    t = re.search(r"dram_bytes_per_launch_full_size:\s*([0-9.eE+]+)", txt)
+    src = re.search(r"source_file:\s*(\S+)", txt)
+    if not (m and t and src):
+        return None
+    cur = hashlib.sha256(open(os.path.join(ROOT, src.group(1)), "rb").read()).hexdigest()
+    return float(t.group(1)) if cur == m.group(1) else None
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _bits(t):
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def host_request(spec, src, r, idx_keys=None):
+    """The oracle's inputs for request r as numpy (pages renumbered 0..n-1)."""
+    npg = spec.pages_per_request()[r]
+    pages = src["page_table"][r, :npg].long()
+    npi = {
+        "q_idx": _bits(src["q_idx"][r:r + 1]),
+        "q": _bits(src["q"][r:r + 1]),
+        "k_cache": _bits(src["k_cache"][pages]),
+        "v_cache": _bits(src["v_cache"][pages]),
+        "k_scale": _bits(src["k_scale"]),
+        "v_scale": _bits(src["v_scale"]),
+        "page_table": np.arange(npg, dtype=np.int32)[None],
+        "q_pos": _bits(src["q_pos"][r:r + 1]),
+    }
+    return npi
+
+
+def oracle_steps(spec, src, idx_keys_fn, n_steps=None, seconds=None):
+    """Time the oracle's decode step one request at a time (inputs copied to
+    host and compressed keys prepared outside the timing). Returns (bytes,
+    seconds, requests)."""
+    from oracle import qsa_oracle as O
+
+    tot_b = 0
+    tot_s = 0.0
+    done = 0
+    r = 0
+    while True:
+        if n_steps is not None and done >= n_steps:
+            break
+        if seconds is not None and tot_s >= seconds and done > 0:
+            break
+        rr = r % spec.batch
+        npi = host_request(spec, src, rr)
+        npi["kc"] = O.compress_keys(idx_keys_fn(rr), spec.max_blocks())[None]
+        t0 = time.perf_counter()
+        res = O.decode_step(npi, spec.kv_dtype, rows=[(0, j) for j in range(spec.n_q)])
+        tot_s += time.perf_counter() - t0
+        nb = (max(spec.q_pos()[rr]) + 1) // 4
+        sel = np.stack([res["sel_pos"][(0, j)] for j in range(spec.n_q)])
+        valid = sel[sel >= 0]
+        tot_b += nb * spec.n_idx_heads * spec.head_dim * 2 + np.unique(valid).size * 2 * kv_row_bytes(spec)
+        done += 1
+        r += 1
+    return tot_b, tot_s, done
+
+
+def run_ours(args, world, rank):
+    qsa = build_lib()
+    spec = synth.spec_for(args.config, batch=args.batch, ctx=args.ctx)
+    st = make_gpu_state(qsa, spec)
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = None if args.no_flush else torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
+
+    # one checked step: its selection gives the byte count
+    d = st["d"]
+    qsa.decode(d, st["g"]["q_idx"], st["kc"], st["g"]["q"], st["g"]["k_cache"], st["g"]["v_cache"],
+               st["g"]["k_scale"], st["g"]["v_scale"], st["g"]["page_table"], st["g"]["q_pos"], st["out"],
+               st["ws"], scores=st["scores"], sel_blk=st["sel_blk"], sel_pos=st["sel_pos"])
+    status, info = qsa.check_errors(st["ws"])
+    if status != qsa.OK:
+        raise RuntimeError(f"device error during the step: {info}")
+    sel_host = st["sel_pos"].cpu().numpy()
+    b_kc = kc_bytes(spec)
+    b_kv_union, b_kv_sum = kv_bytes(spec, sel_host)
+    bytes_step = b_kc + b_kv_union
+
+    # warm-up, then exactly K timed steps
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush.zero_()
+        decode_call(qsa, st)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("start")
+    step_ms = timed(lambda: decode_call(qsa, st), args.steps, flush, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    if sampler:
+        sampler.mark("stop")
+    clocks = sampler.stop() if sampler else None
+    ms_local = sum(step_ms) / len(step_ms)
+    ms = max_over_ranks(ms_local, world)
+    value = bytes_step * world / (ms * 1e-3) / 1e9
+
+    # per-kernel device times through each kernel's own entry point (same inputs, same flush)
+    g = st["g"]
+    reps = max(20, min(args.steps, 200))
+    k_ms = {
+        "score": statistics.mean(timed(lambda: qsa.score(d, g["q_idx"], st["kc"], g["q_pos"], st["scores"], st["ws"]),
+                                       reps, flush, stream)),
+        "topk": statistics.mean(timed(lambda: qsa.topk(d, st["scores"], g["q_pos"], st["sel_blk"], st["sel_pos"],
+                                                       st["ws"]), reps, flush, stream)),
+        "sparse_attn": statistics.mean(timed(lambda: qsa.sparse_attn(d, g["q"], g["k_cache"], g["v_cache"],
+                                                                     g["k_scale"], g["v_scale"], g["page_table"],
+                                                                     st["sel_pos"], g["q_pos"], st["out"], st["ws"]),
+                                             reps, flush, stream)),
+    }
+    k_bytes = {
+        "score": b_kc + sum((p + 1) // 4 for qp in spec.q_pos() for p in qp) * 4,
+        "topk": sum((p + 1) // 4 for qp in spec.q_pos() for p in qp) * 4 + spec.batch * spec.n_q * (512 + 2051) * 4,
+        "sparse_attn": b_kv_union,
+    }
+    kernels = {k: {"us": round(v * 1e3, 2), "alg_bytes": int(k_bytes[k]),
+                   "gbs": round(k_bytes[k] / (v * 1e-3) / 1e9, 1)} for k, v in k_ms.items()}
+    dom = max(k_ms, key=lambda k: k_ms[k])
+    peak, peak_kind = peaks()
+    tags = {"score": "score_kernel_verify_b32_ctx50k", "topk": "topk_kernel_verify_b32_ctx50k",
+            "sparse_attn": "attn_kernel_verify_b32_ctx50k_bf16"}
+    traffic = ncu_traffic(tags[dom]) if args.config == 2 and args.batch in (None, 32) else None
+    achieved = k_bytes[dom] / (k_ms[dom] * 1e-3) / 1e9
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
+                "traffic": traffic, "alg_bytes_per_launch": int(k_bytes[dom]),
+                "step_frac": round(value / world / peak, 4)}
+
+    # end to end through the public API with host buffers
+    per_step = ["q_idx", "q", "q_pos", "page_table"]
+    host = {k: g[k].cpu().pin_memory() for k in per_step}
+    dev_in = {k: torch.empty_like(g[k]) for k in per_step}
+    out_host = torch.empty(st["out"].shape, dtype=st["out"].dtype).pin_memory()
+    h2d = sum(host[k].numel() * host[k].element_size() for k in per_step)
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for k in per_step:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        decode_call(qsa, st, inputs=dev_in)
+        out_host.copy_(st["out"], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    e2e_ms = statistics.mean(timed(e2e_step, reps, flush, stream))
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    e2e = {"value": round(bytes_step * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+           "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        idx_keys = synth.normal_bf16((spec.batch, 4 * spec.max_blocks(), spec.n_idx_heads, spec.head_dim),
+                                     spec.seed + synth.T_IDXKEYS, device="cuda")
+        b, s, n = oracle_steps(spec, g, lambda r: _bits(idx_keys[r]), seconds=args.cpu_seconds)
+        del idx_keys
+        cpu = {"value": round(b / s / 1e9, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n} of {spec.batch} requests (all {spec.n_q} queries each), one at a time, numpy FP64",
+               "seconds": round(s, 2)}
+
+    if rank == 0:
+        res = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 5), "latency_us": round(ms * 1e3, 2),
+            "latency_us_p10_p50_p90": [round(float(np.percentile(step_ms, q)) * 1e3, 2) for q in (10, 50, 90)],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8" if spec.kv_dtype == "fp8" else "bf16", "data": "synthetic",
+            "config": {"workload": spec.name, "batch": spec.batch, "n_q": spec.n_q,
+                       "contexts": "50000+800*t, t~U{0..14}" if args.config in (2, 3) else str(spec.first_pos[0]),
+                       "n_idx_heads": spec.n_idx_heads, "kv": spec.kv_dtype, "page_size": spec.page_size,
+                       "l2": "no flush (warm)" if flush is None else "flushed before every step (write of 2x L2)",
+                       "parallelism": f"replicas x{world}"},
+            "bytes_per_step": {"kc": int(b_kc), "kv_union": int(b_kv_union), "kv_sum": int(b_kv_sum)},
+            "kernels": kernels, "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": 3 * args.steps, "clocks": clocks,
+        }
+        print(json.dumps(res))
+
+
+def run_reference(args, world, rank):
+    """The oracle as it stands, timed on the host cores, one request per step."""
+    if rank != 0:
+        return
+    spec = synth.spec_for(args.config, batch=args.batch, ctx=args.ctx)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    g = synth.make_inputs(spec, device=dev, with_index_keys=False)
+    idx_keys = synth.normal_bf16((spec.batch, 4 * spec.max_blocks(), spec.n_idx_heads, spec.head_dim),
+                                 spec.seed + synth.T_IDXKEYS, device=dev)
+    kfn = lambda r: _bits(idx_keys[r])  # noqa: E731
+    oracle_steps(spec, g, kfn, n_steps=args.warmup)
+    b, s, n = oracle_steps(spec, g, kfn, n_steps=args.steps)
+    value = b / s / 1e9
+    res = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s / n * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": spec.name, "batch": spec.batch, "n_q": spec.n_q, "kv": spec.kv_dtype,
+                   "step": "one request (all its queries) of the batch, cycling"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{n} requests of {spec.name}, one per step, numpy FP64 single-threaded"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(res))
+
+
+def main():
+    args = parse_args()
+    world, rank, _ = dist_init()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

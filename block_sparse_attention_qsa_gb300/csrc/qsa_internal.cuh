@@ -1,0 +1,106 @@
+// Internal declarations shared by the libqsa translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+
+#include "qsa.h"
+
+namespace qsa {
+
+constexpr int kBlock = 4;        // tokens per micro-block
+constexpr int kTopK = 512;       // selected full blocks per query
+constexpr int kWidth = 2051;     // selection buffer width: 512 * 4 + 3
+constexpr int kDim = 128;        // index and attention head dim
+constexpr int kGroup = 8;        // query heads per KV head
+constexpr int kMaxNq = 4;        // verify queries per request
+
+// Device error kinds recorded in the workspace header.
+enum DevErr : int32_t { kErrNone = 0, kErrQueryPos = 1, kErrPage = 2, kErrSelPos = 3 };
+
+// ---------------------------------------------------------------------------
+// Workspace layout (byte offsets from the 256-aligned base).
+//   [0, 256)           header: int32 err_kind, err_request, err_query, err_value
+//   tickets            int32 [units]           split-KV arrival counters
+//   partials           float [units][nsplit][kPartFloats]
+//   scores (decode)    float [B][n_q][max_blocks]
+//   sel_blk (decode)   int32 [B][n_q][512]
+//   sel_pos (decode)   int32 [B][n_q][2051]
+// ---------------------------------------------------------------------------
+constexpr int kPartFloats = 2 * kGroup + kGroup * kDim;  // m[8], l[8], acc[8][128]
+
+struct WsLayout {
+  size_t tickets, partials, scores, sel_blk, sel_pos, total;
+  int units, nsplit, tiles_per_split;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Split-KV plan for the attention kernel (shared by sizing and launch).
+struct AttnPlan {
+  int units;            // batch * n_q * n_kv_heads
+  int nsplit;           // CTAs per unit
+  int tiles_per_split;  // 64-position tiles per CTA
+};
+AttnPlan attn_plan(const qsa_dims& d, int num_sms);
+WsLayout ws_layout(const qsa_dims& d, int num_sms);
+
+int device_sm_count();
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void record_error(int32_t* hdr, int32_t kind, int32_t r, int32_t j,
+                                             int32_t value) {
+  if (atomicCAS(hdr, 0, kind) == 0) {
+    hdr[1] = r;
+    hdr[2] = j;
+    hdr[3] = value;
+  }
+}
+
+__device__ __forceinline__ int n_full_of(int p) { return (p + 1) >> 2; }
+
+// ---------------------------------------------------------------------------
+// host-side launch helper: cudaLaunchKernelEx with optional PDL attribute
+// ---------------------------------------------------------------------------
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// ---------------------------------------------------------------------------
+// launchers implemented in the kernel translation units
+// ---------------------------------------------------------------------------
+cudaError_t launch_compress(const qsa_dims& d, const __nv_bfloat16* idx_keys, const int32_t* q_pos,
+                            const int32_t* block_lo, __nv_bfloat16* kc, int32_t* err,
+                            cudaStream_t s);
+cudaError_t launch_score(const qsa_dims& d, const __nv_bfloat16* q_idx, const __nv_bfloat16* kc,
+                         const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s, bool pdl);
+cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q_pos,
+                        int32_t* sel_blk, int32_t* sel_pos, int32_t* err, cudaStream_t s, bool pdl);
+cudaError_t launch_attn(const qsa_dims& d, const void* q, const void* k_cache, const void* v_cache,
+                        const float* k_scale, const float* v_scale, const int32_t* page_table,
+                        const int32_t* sel_pos, const int32_t* q_pos, void* out, int32_t* err,
+                        int32_t* tickets, float* partials, const AttnPlan& plan, cudaStream_t s,
+                        bool pdl);
+
+}  // namespace qsa

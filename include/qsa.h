@@ -1,0 +1,197 @@
+/*
+ * qsa.h -- C ABI of libqsa.so: the decode / MTP-verify step of Qwen Sparse
+ * Attention (QSA) on one GB300 (sm_103a).
+ *
+ * The step, as the pages state it (arex-research.com, "LightSeek 公告
+ * TokenSpeed 服务 Qwen3.8-Flash-Next ...", section "稀疏选择、CuTe DSL 内核与
+ * MTP 复用：四类优化", bullets 1-4; 10100.com, section "第一处"):
+ *   1. tokens form micro-blocks of 4; each block has a compressed index key;
+ *   2. every full block is scored against each query's index query and the
+ *      scores go to an FP32 buffer; up to 4 verify queries of one request
+ *      share each compressed-key tile load (bullet 2);
+ *   3. a persistent radix selector keeps the top 512 blocks per query; the
+ *      current unfilled block is kept without selection; the selection buffer
+ *      is 2,051 positions wide (bullet 1);
+ *   4. sparse attention over the selected positions with a BF16 query and a
+ *      BF16 or FP8-E4M3 KV cache (bullet 3); the three kernels are chained
+ *      with programmatic dependent launch (bullet 4).
+ *
+ * Readings where the pages are silent:
+ *   - full blocks of a query at position p: b < (p + 1) / 4; the unfilled
+ *     block holds positions 4 * ((p + 1) / 4) .. p, (p + 1) % 4 of them;
+ *   - compressed key = FP32 mean of the block's 4 BF16 index keys, summed in
+ *     token order, rounded to BF16 (qsa_compress_keys);
+ *   - score = dot(index query, compressed key) summed over index heads, FP32;
+ *   - top-k ties go to the lower block index; -0.0 == +0.0; NaN ranks last;
+ *   - the selection buffer lists selected blocks ascending (4 positions
+ *     each), then the unfilled block's positions, then -1;
+ *   - query head h reads KV head h / (n_q_heads / n_kv_heads); softmax scale
+ *     sm_scale (default 1/sqrt(head_dim)); FP8 values are code * scale with
+ *     one FP32 scale per KV head, separate for K and V.
+ *
+ * Layouts (all row-major, all device memory owned by the caller):
+ *   q_idx      bf16  [batch][n_q][n_idx_heads][idx_dim]
+ *   idx_keys   bf16  [batch][4 * max_blocks][n_idx_heads][idx_dim]
+ *   kc         bf16  [batch][max_blocks][n_idx_heads][idx_dim]
+ *   q_pos      int32 [batch][n_q]        position of each query token; the
+ *                                        query's own K/V is already cached
+ *   scores     fp32  [batch][n_q][max_blocks]   (entries past a query's
+ *                                        full blocks are left untouched)
+ *   sel_blk    int32 [batch][n_q][topk]  ascending, -1 padded
+ *   sel_pos    int32 [batch][n_q][width] ascending, -1 padded
+ *   q, out     bf16  [batch][n_q][n_q_heads][head_dim]
+ *   k_cache, v_cache  bf16 or uint8 (E4M3 codes)
+ *                     [num_pages][n_kv_heads][page_size][head_dim]
+ *   k_scale, v_scale  fp32 [n_kv_heads]  (read only for FP8; may be NULL
+ *                                         for BF16)
+ *   page_table int32 [batch][max_pages]  token t of request r lives in page
+ *                                        page_table[r][t / page_size], slot
+ *                                        t % page_size
+ *
+ * Execution: every call is asynchronous on `stream` (a cudaStream_t passed as
+ * void*; NULL = the legacy default stream) and allocates nothing. Argument
+ * and shape errors return synchronously before anything is launched.
+ * Data-dependent errors found on the device (a query position outside the
+ * buffers, a page id outside the cache, a selected position after its query)
+ * are recorded in the workspace header and the offending item is skipped (a
+ * query with a bad position gets no scores, an all -1 selection and a zero
+ * output; a bad selected position or page is left out of the softmax);
+ * qsa_check_errors() reports them. No call aborts or throws.
+ *
+ * Workspace: every entry point takes `ws`, a caller-owned device buffer of at
+ * least qsa_workspace_size() bytes, 256-byte aligned, zero-filled once before
+ * its first use (qsa_workspace_init). The kernels leave it in a state ready
+ * for the next call. Calls that share a workspace must not overlap on the
+ * GPU (issue them on one stream).
+ *
+ * Supported geometry: idx_dim == head_dim == 128, n_q in 1..4,
+ * n_idx_heads in 1..4, n_q_heads == 8 * n_kv_heads, block == 4, topk == 512,
+ * width == 2051, page_size a power of two in 16..256; anything else returns
+ * QSA_ERR_UNSUPPORTED.
+ */
+#ifndef QSA_H_
+#define QSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QSA_ABI_VERSION 1
+
+typedef enum {
+  QSA_OK = 0,
+  QSA_ERR_INVALID_ARG = 1, /* null pointer, bad size or stride */
+  QSA_ERR_UNSUPPORTED = 2, /* geometry outside the supported set */
+  QSA_ERR_WORKSPACE = 3,   /* ws too small or misaligned */
+  QSA_ERR_BAD_INDEX = 4,   /* device found an out-of-range position/page */
+  QSA_ERR_TIMEOUT = 5,     /* a bounded device wait gave up */
+  QSA_ERR_CUDA = 6         /* a CUDA runtime call failed */
+} qsa_status;
+
+typedef enum { QSA_KV_BF16 = 0, QSA_KV_FP8_E4M3 = 1 } qsa_kv_dtype;
+
+typedef struct {
+  int32_t batch;       /* requests in the step, >= 1 */
+  int32_t n_q;         /* query tokens per request (1 decode, 4 verify) */
+  int32_t n_idx_heads; /* index heads whose scores are summed */
+  int32_t idx_dim;     /* index head dim, 128 */
+  int32_t n_q_heads;   /* attention query heads, 16 */
+  int32_t n_kv_heads;  /* attention KV heads, 2 */
+  int32_t head_dim;    /* 128 */
+  int32_t page_size;   /* tokens per KV page, 64 */
+  int32_t max_blocks;  /* row stride (in blocks) of kc and scores */
+  int32_t max_pages;   /* row stride of page_table */
+  int32_t num_pages;   /* pages in k_cache / v_cache */
+  int32_t topk;        /* 512 */
+  int32_t block;       /* 4 */
+  int32_t width;       /* selection width, topk * block + block - 1 = 2051 */
+  float sm_scale;      /* softmax scale; 0 selects 1/sqrt(head_dim) */
+  int32_t kv_dtype;    /* qsa_kv_dtype */
+} qsa_dims;
+
+/* ABI version of the loaded library (QSA_ABI_VERSION it was built with). */
+int32_t qsa_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* qsa_status_str(qsa_status s);
+
+/* Fill `dims` with the defaults of the pages' geometry (16/2 heads of 128,
+ * 1 index head of 128, pages of 64, top-512 of 4-token blocks, width 2,051,
+ * BF16 KV); the caller then sets batch, n_q, max_blocks, max_pages,
+ * num_pages and anything else it changes. */
+void qsa_dims_default(qsa_dims* dims);
+
+/* Bytes of workspace the entry points need for `dims` on the current device.
+ * The size depends on the device's SM count (it sizes split-KV scratch). */
+qsa_status qsa_workspace_size(const qsa_dims* dims, size_t* bytes);
+
+/* Zero `ws` (ws_bytes bytes) on `stream`. Required once after allocating a
+ * workspace; the kernels keep it clean afterwards. */
+qsa_status qsa_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Compressed index key of each full block (the pages' bullet 1 "compute a
+ * compressed index key per micro-block"; the formula is this library's
+ * reading: FP32 mean of the 4 keys, summed in token order, rounded to BF16).
+ * For request r, writes kc[r][b] for block_lo[r] <= b < (P_r + 1) / 4 where
+ * P_r = max_j q_pos[r][j]; block_lo may be NULL (= 0 for every request), so
+ * an engine can refresh only the blocks its newest tokens completed. */
+qsa_status qsa_compress_keys(const qsa_dims* dims, const void* idx_keys, const int32_t* q_pos,
+                             const int32_t* block_lo, void* kc, void* ws, size_t ws_bytes,
+                             void* stream);
+
+/* Step 1: FP32 block scores (bullet 1: "block scores are written to an FP32
+ * buffer"; bullet 2: up to 4 queries of a request share one compressed-key
+ * load). For each request r, query j at p = q_pos[r][j] and full block
+ * b < (p + 1) / 4: scores[r][j][b] = sum_h sum_d q_idx[r][j][h][d] *
+ * kc[r][b][h][d] in FP32. Each compressed key is read from HBM once per
+ * request and used for all n_q queries. */
+qsa_status qsa_score(const qsa_dims* dims, const void* q_idx, const void* kc, const int32_t* q_pos,
+                     float* scores, void* ws, size_t ws_bytes, void* stream);
+
+/* Steps 2-3: top-k block selection and the selection buffer (bullet 1:
+ * persistent radix selector over the FP32 scores, at most 512 full blocks,
+ * the unfilled block kept, width 2,051). For each (r, j): sel_blk = the
+ * min(topk, n_full) highest-scoring full blocks, ties to the lower index,
+ * ascending, -1 padded; sel_pos = their positions 4b..4b+3 ascending, then
+ * 4 * n_full .. p, then -1 up to width. Bit-exact and deterministic. */
+qsa_status qsa_topk(const qsa_dims* dims, const float* scores, const int32_t* q_pos,
+                    int32_t* sel_blk, int32_t* sel_pos, void* ws, size_t ws_bytes, void* stream);
+
+/* Step 4: sparse attention over the selected positions (bullet 3: BF16
+ * query, BF16 or FP8-E4M3 KV cache, decode and MTP verify). For each (r, j)
+ * and query head h with KV head g = h / (n_q_heads / n_kv_heads):
+ * out = softmax(sm_scale * q K^T) V over the positions t >= 0 of
+ * sel_pos[r][j], with K, V read through page_table (times k_scale[g] /
+ * v_scale[g] for FP8). FP32 softmax statistics and accumulation, BF16 out.
+ * A selected position after q_pos[r][j] (a causality violation) or one whose
+ * page id is outside the cache is reported and skipped. */
+qsa_status qsa_sparse_attn(const qsa_dims* dims, const void* q, const void* k_cache,
+                           const void* v_cache, const float* k_scale, const float* v_scale,
+                           const int32_t* page_table, const int32_t* sel_pos, const int32_t* q_pos,
+                           void* out, void* ws, size_t ws_bytes, void* stream);
+
+/* The fused step (bullet 4: "QSA logits -> select -> attention" chained with
+ * programmatic dependent launch): qsa_score, qsa_topk and qsa_sparse_attn
+ * back to back on `stream`. scores, sel_blk and sel_pos are optional outputs:
+ * NULL keeps them in the workspace. */
+qsa_status qsa_decode(const qsa_dims* dims, const void* q_idx, const void* kc, const void* q,
+                      const void* k_cache, const void* v_cache, const float* k_scale,
+                      const float* v_scale, const int32_t* page_table, const int32_t* q_pos,
+                      float* scores, int32_t* sel_blk, int32_t* sel_pos, void* out, void* ws,
+                      size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, reads and clears the device error record in `ws`.
+ * Returns QSA_OK if no device-side error was recorded since the last check,
+ * else QSA_ERR_BAD_INDEX (or QSA_ERR_TIMEOUT). `info` (may be NULL) receives
+ * 4 int32: error kind (1 query position, 2 page id, 3 selected position),
+ * request, query, offending value. */
+qsa_status qsa_check_errors(void* ws, void* stream, int32_t* info);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H_ */

@@ -1,0 +1,494 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Tolerances (stated by the step's contract and restated here):
+  * compressed keys, top-k block ids and selection buffers: bit-exact;
+  * scores: |gpu - ref| <= 1e-4 * max(|ref|, 1);
+  * attention outputs: max-abs <= 1e-2 with BF16 KV, <= 3e-2 with FP8 KV
+    (the oracle decodes the same E4M3 bytes and scales).
+Top-k is bit-exact when both sides start from the same FP32 score buffer, so
+its unit tests feed both sides seeded score buffers. End to end, the oracle
+recomputes everything from the generator's inputs; a row whose 512th and
+513th oracle scores are closer than the score tolerance can legitimately
+select differently and is counted, not compared.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from block_sparse_attention_qsa_gb300 import synth
+from oracle import qsa_oracle as O
+from tests._util import bits, small_spec, to_numpy_inputs
+
+pytestmark = pytest.mark.gpu
+
+SCORE_RTOL = 1e-4
+ATOL = {"bf16": 1e-2, "fp8": 3e-2}
+
+
+@pytest.fixture(scope="module")
+def qsa():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    from block_sparse_attention_qsa_gb300 import qsa as q
+
+    return q
+
+
+def _dev(inp):
+    return {k: v.cuda() for k, v in inp.items()}
+
+
+def _kc_oracle(npi, spec):
+    return np.stack([O.compress_keys(npi["idx_keys"][r], spec.max_blocks()) for r in range(spec.batch)])
+
+
+def _bf16_tensor(bits_u16):
+    return torch.from_numpy(np.ascontiguousarray(bits_u16).view(np.int16)).view(torch.bfloat16)
+
+
+def _check_ok(qsa, ws):
+    st, info = qsa.check_errors(ws)
+    assert st == qsa.OK, info
+
+
+SPECS = {
+    "b2-h1-bf16": lambda: small_spec([3001, 1498], n_q=4, seed=5),
+    "b3-h4-fp8": lambda: small_spec([2600, 4097, 77], n_q=4, n_idx_heads=4, kv_dtype="fp8", seed=6),
+    "b1-nq1-h2": lambda: small_spec([5003], n_q=1, n_idx_heads=2, seed=7),
+    "b2-nq3-h3": lambda: small_spec([2100, 3333], n_q=3, n_idx_heads=3, seed=8),
+    "b2-nq2-h1-fp8": lambda: small_spec([9000, 2050], n_q=2, kv_dtype="fp8", seed=9),
+}
+
+
+# --------------------------------------------------------------------------
+# per-stage parity on small specs (several tiles, ragged tails)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", list(SPECS))
+def test_compress_keys_bit_exact(qsa, name):
+    spec = SPECS[name]()
+    inp = synth.make_inputs(spec)
+    npi = to_numpy_inputs(inp)
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    g = _dev(inp)
+    kc = torch.zeros((spec.batch, spec.max_blocks(), spec.n_idx_heads, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.compress_keys(d, g["idx_keys"], g["q_pos"], kc, ws)
+    _check_ok(qsa, ws)
+    ref = _kc_oracle(npi, spec)
+    got = bits(kc)
+    for r in range(spec.batch):
+        nb = O.n_full(max(spec.q_pos()[r]))
+        assert np.array_equal(got[r, :nb], ref[r, :nb])
+        assert np.all(got[r, nb:] == 0)  # blocks not yet full are left alone
+
+
+def test_compress_keys_block_lo_refreshes_only_new_blocks(qsa):
+    spec = small_spec([3001, 1498], n_q=4, seed=15)
+    inp = synth.make_inputs(spec)
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    g = _dev(inp)
+    kc = torch.zeros((2, spec.max_blocks(), 1, 128), dtype=torch.bfloat16, device="cuda")
+    lo = torch.tensor([700, 100], dtype=torch.int32, device="cuda")
+    qsa.compress_keys(d, g["idx_keys"], g["q_pos"], kc, ws, block_lo=lo)
+    _check_ok(qsa, ws)
+    ref = _kc_oracle(to_numpy_inputs(inp), spec)
+    got = bits(kc)
+    assert np.all(got[0, :700] == 0) and np.array_equal(got[0, 700:751], ref[0, 700:751])
+    assert np.all(got[1, :100] == 0) and np.array_equal(got[1, 100:375], ref[1, 100:375])
+
+
+@pytest.mark.parametrize("name", list(SPECS))
+def test_score_parity(qsa, name):
+    spec = SPECS[name]()
+    inp = synth.make_inputs(spec)
+    npi = to_numpy_inputs(inp)
+    npi["kc"] = _kc_oracle(npi, spec)
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    g = _dev(inp)
+    kc = _bf16_tensor(npi["kc"]).cuda()
+    scores = torch.full((spec.batch, spec.n_q, spec.max_blocks()), float("nan"), device="cuda")
+    qsa.score(d, g["q_idx"], kc, g["q_pos"], scores, ws)
+    _check_ok(qsa, ws)
+    got = scores.cpu().numpy()
+    for r in range(spec.batch):
+        for j in range(spec.n_q):
+            p = spec.q_pos()[r][j]
+            ref = O.score_row(npi["q_idx"][r, j], npi["kc"][r], p)
+            nb = ref.shape[0]
+            err = np.abs(got[r, j, :nb].astype(np.float64) - ref) / np.maximum(np.abs(ref), 1.0)
+            assert err.max() <= SCORE_RTOL, (r, j, err.max())
+            assert np.all(np.isnan(got[r, j, nb:]))  # nothing written past the full blocks
+
+
+def _score_rows(kind, n, seed):
+    rng = np.random.default_rng(seed)
+    if kind == "normal":
+        return (rng.standard_normal(n) * 5.7).astype(np.float32)
+    if kind == "all_equal":
+        return np.full(n, 1.5, np.float32)
+    if kind == "two_values":
+        return np.where(rng.random(n) < 0.3, 2.0, -1.0).astype(np.float32)
+    if kind == "ascending":
+        return np.arange(n, dtype=np.float32)
+    if kind == "descending":
+        return np.arange(n, dtype=np.float32)[::-1].copy()
+    if kind == "signed_zeros":
+        z = np.zeros(n, np.float32)
+        z[::2] = -0.0
+        z[3::11] = -2.0
+        z[5::13] = 1.0
+        return z
+    if kind == "exact_512_top":
+        z = np.full(n, -3.0, np.float32)
+        z[rng.choice(n, 512, replace=False)] = 7.0
+        return z
+    if kind == "ties_at_threshold":
+        z = (rng.standard_normal(n) - 10).astype(np.float32)
+        z[rng.choice(n, 300, replace=False)] = 50.0
+        idx = rng.choice(np.nonzero(z < 0)[0], 600, replace=False)
+        z[idx] = 1.25  # 600 tied, 212 taken
+        return z
+    if kind == "few_bits":
+        # values that agree in their top 22 key bits: exercises the last pass
+        base = np.float32(3.0).view(np.uint32)
+        return (base + rng.integers(0, 1024, n).astype(np.uint32)).view(np.float32)
+    if kind == "with_nan":
+        z = rng.standard_normal(n).astype(np.float32)
+        z[::5] = np.nan
+        return z
+    raise ValueError(kind)
+
+
+TOPK_CASES = [
+    ("normal", 0), ("normal", 1), ("normal", 511), ("normal", 512), ("normal", 513),
+    ("normal", 12501), ("normal", 15301), ("normal", 65537),
+    ("all_equal", 2000), ("all_equal", 65537), ("two_values", 9000), ("ascending", 5000),
+    ("descending", 5000), ("signed_zeros", 4000), ("exact_512_top", 7000),
+    ("ties_at_threshold", 6000), ("few_bits", 3000), ("few_bits", 60000), ("with_nan", 3000),
+]
+
+
+@pytest.mark.parametrize("kind,n", TOPK_CASES)
+def test_topk_bit_exact_on_shared_scores(qsa, kind, n):
+    # 2 requests x 2 queries: rows of n and a shorter ragged row per request
+    n_q = 2
+    mb = max(n, 1)
+    lens = [[n, max(0, n - 37)], [max(0, n // 3), n]]
+    # query k of a row with L full blocks sits at 4L + k - 1 (k partial tokens)
+    q_pos = [[max(0, 4 * L + k - 1) for k, L in enumerate(row)] for row in lens]
+    for row in q_pos:
+        for p in row:
+            assert O.n_full(p) <= mb
+    scores = np.stack([np.stack([_score_rows(kind, mb, 100 * r + j) for j in range(n_q)]) for r in range(2)])
+    d = qsa.make_dims(2, n_q, mb, 1, 1)
+    ws = qsa.make_workspace(d)
+    sc = torch.from_numpy(scores).cuda()
+    qp = torch.tensor(q_pos, dtype=torch.int32, device="cuda")
+    sb = torch.full((2, n_q, 512), 7, dtype=torch.int32, device="cuda")
+    sp = torch.full((2, n_q, 2051), 7, dtype=torch.int32, device="cuda")
+    qsa.topk(d, sc, qp, sb, sp, ws)
+    _check_ok(qsa, ws)
+    gb, gp = sb.cpu().numpy(), sp.cpu().numpy()
+    for r in range(2):
+        for j in range(n_q):
+            p = q_pos[r][j]
+            ref_b = O.topk_blocks(scores[r, j, : O.n_full(p)])
+            assert np.array_equal(gb[r, j], ref_b), (r, j)
+            assert np.array_equal(gp[r, j], O.select_positions(ref_b, p)), (r, j)
+
+
+def test_topk_is_deterministic_across_runs(qsa):
+    n = 20000
+    scores = np.stack([_score_rows("two_values", n, 3)])[None]
+    d = qsa.make_dims(1, 1, n, 1, 1)
+    ws = qsa.make_workspace(d)
+    sc = torch.from_numpy(scores).cuda()
+    qp = torch.tensor([[4 * n - 1]], dtype=torch.int32, device="cuda")
+    outs = []
+    for _ in range(3):
+        sb = torch.empty((1, 1, 512), dtype=torch.int32, device="cuda")
+        sp = torch.empty((1, 1, 2051), dtype=torch.int32, device="cuda")
+        qsa.topk(d, sc, qp, sb, sp, ws)
+        outs.append((sb.cpu(), sp.cpu()))
+    assert all(torch.equal(outs[0][0], o[0]) and torch.equal(outs[0][1], o[1]) for o in outs)
+
+
+@pytest.mark.parametrize("name", list(SPECS))
+def test_sparse_attn_parity_on_oracle_selection(qsa, name):
+    spec = SPECS[name]()
+    inp = synth.make_inputs(spec)
+    npi = to_numpy_inputs(inp)
+    npi["kc"] = _kc_oracle(npi, spec)
+    res = O.decode_step(npi, spec.kv_dtype)
+    sel = np.stack([np.stack([res["sel_pos"][(r, j)] for j in range(spec.n_q)]) for r in range(spec.batch)])
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    g = _dev(inp)
+    out = torch.full((spec.batch, spec.n_q, 16, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    qsa.sparse_attn(d, g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"], g["page_table"],
+                    torch.from_numpy(sel).cuda(), g["q_pos"], out, ws)
+    _check_ok(qsa, ws)
+    got = out.float().cpu().numpy()
+    for r in range(spec.batch):
+        for j in range(spec.n_q):
+            err = np.max(np.abs(got[r, j] - res["out"][(r, j)]))
+            assert err <= ATOL[spec.kv_dtype], (r, j, err)
+
+
+def test_sparse_attn_with_holes_and_single_positions(qsa):
+    spec = small_spec([4000, 130], n_q=2, seed=21)
+    inp = synth.make_inputs(spec)
+    npi = to_numpy_inputs(inp)
+    rng = np.random.default_rng(4)
+    sel = np.full((2, 2, 2051), -1, np.int32)
+    sel[0, 0, :1500] = np.sort(rng.choice(4001, 1500, replace=False))
+    sel[0, 0, rng.choice(1500, 300, replace=False)] = -1  # holes anywhere
+    sel[0, 1, 0] = 4001  # a single position
+    sel[1, 0, 1000] = 17  # a single position late in the buffer
+    sel[1, 1, :131] = np.arange(131)[::-1]  # any order
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    g = _dev(inp)
+    out = torch.empty((2, 2, 16, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.sparse_attn(d, g["q"], g["k_cache"], g["v_cache"], None, None, g["page_table"],
+                    torch.from_numpy(sel).cuda(), g["q_pos"], out, ws)
+    _check_ok(qsa, ws)
+    got = out.float().cpu().numpy()
+    for r in range(2):
+        for j in range(2):
+            ref = O.sparse_attn(npi["q"][r, j], npi["k_cache"], npi["v_cache"], npi["page_table"][r], sel[r, j])
+            assert np.max(np.abs(got[r, j] - ref)) <= 1e-2
+
+
+# --------------------------------------------------------------------------
+# the fused step, chained stage by stage
+# --------------------------------------------------------------------------
+
+def _near_tie(scores_row, k=512, tol=SCORE_RTOL):
+    if scores_row.shape[0] <= k:
+        return False
+    s = np.sort(scores_row.astype(np.float64))[::-1]
+    return (s[k - 1] - s[k]) <= 2 * tol * max(abs(s[k - 1]), 1.0)
+
+
+def _decode_and_compare(qsa, spec, rows=None, gpu_inputs=None):
+    """Run qsa_decode on the GPU and compare the requested (r, j) rows with
+    the oracle computed from the same generator inputs."""
+    g = gpu_inputs if gpu_inputs is not None else _dev(synth.make_inputs(spec))
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    kc = torch.zeros((spec.batch, spec.max_blocks(), spec.n_idx_heads, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.compress_keys(d, g["idx_keys"], g["q_pos"], kc, ws)
+    scores = torch.empty((spec.batch, spec.n_q, spec.max_blocks()), device="cuda")
+    sb = torch.empty((spec.batch, spec.n_q, 512), dtype=torch.int32, device="cuda")
+    sp = torch.empty((spec.batch, spec.n_q, 2051), dtype=torch.int32, device="cuda")
+    out = torch.empty((spec.batch, spec.n_q, 16, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.decode(d, g["q_idx"], kc, g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"],
+               g["page_table"], g["q_pos"], out, ws, scores=scores, sel_blk=sb, sel_pos=sp)
+    _check_ok(qsa, ws)
+    if rows is None:
+        rows = [(r, j) for r in range(spec.batch) for j in range(spec.n_q)]
+    skipped = 0
+    ks = g["k_scale"].cpu().numpy()
+    vs = g["v_scale"].cpu().numpy()
+    for r in sorted(set(r for r, _ in rows)):
+        # the oracle's own view of request r, copied from the generator's tensors
+        npg = spec.pages_per_request()[r]
+        pages = g["page_table"][r, :npg].long()
+        npi = {
+            "q_idx": bits(g["q_idx"][r : r + 1]),
+            "q": bits(g["q"][r : r + 1]),
+            "k_cache": bits(g["k_cache"][pages]),
+            "v_cache": bits(g["v_cache"][pages]),
+            "k_scale": ks,
+            "v_scale": vs,
+            "page_table": np.arange(npg, dtype=np.int32)[None],
+            "q_pos": bits(g["q_pos"][r : r + 1]),
+        }
+        idx = bits(g["idx_keys"][r])
+        npi["kc"] = O.compress_keys(idx, spec.max_blocks())[None]
+        nb_r = O.n_full(max(spec.q_pos()[r]))
+        assert np.array_equal(bits(kc[r, :nb_r]), npi["kc"][0, :nb_r])
+        for rr, j in rows:
+            if rr != r:
+                continue
+            res = O.decode_step(npi, spec.kv_dtype, rows=[(0, j)])
+            ref_s = res["scores"][(0, j)]
+            got_s = scores[r, j, : ref_s.shape[0]].cpu().numpy().astype(np.float64)
+            assert np.max(np.abs(got_s - ref_s) / np.maximum(np.abs(ref_s), 1.0)) <= SCORE_RTOL
+            if _near_tie(ref_s):
+                skipped += 1
+                continue
+            assert np.array_equal(sb[r, j].cpu().numpy(), res["sel_blk"][(0, j)]), (r, j)
+            assert np.array_equal(sp[r, j].cpu().numpy(), res["sel_pos"][(0, j)]), (r, j)
+            err = np.max(np.abs(out[r, j].float().cpu().numpy() - res["out"][(0, j)]))
+            assert err <= ATOL[spec.kv_dtype], (r, j, err)
+    return skipped, len(rows)
+
+
+@pytest.mark.parametrize("name", list(SPECS))
+def test_decode_small_specs(qsa, name):
+    skipped, n = _decode_and_compare(qsa, SPECS[name]())
+    assert skipped <= max(1, n // 10)
+
+
+@pytest.mark.parametrize("config", [0, 1])
+def test_decode_full_size_batch1_configs(qsa, config):
+    spec = synth.spec_for(config)
+    skipped, n = _decode_and_compare(qsa, spec)
+    assert skipped <= 1
+
+
+@pytest.mark.parametrize("config", [2, 3])
+def test_decode_full_size_batch32_sampled_rows(qsa, config):
+    spec = synth.spec_for(config)
+    rows = [(0, 0), (5, 1), (11, 2), (17, 3), (31, 0), (31, 3), (23, 2)]
+    skipped, n = _decode_and_compare(qsa, spec, rows=rows)
+    assert skipped <= 1
+
+
+def test_decode_long_context_batch1_sampled(qsa):
+    spec = synth.spec_for(4, batch=1, ctx=131072)
+    skipped, n = _decode_and_compare(qsa, spec, rows=[(0, 0), (0, 3)])
+    assert skipped <= 1
+
+
+def test_decode_long_context_262k_row_over_shared_memory(qsa):
+    # 65,537 full blocks: the selector's keys no longer fit in shared memory
+    spec = synth.spec_for(4, batch=1, ctx=262144)
+    skipped, n = _decode_and_compare(qsa, spec, rows=[(0, 3)])
+    assert skipped <= 1
+
+
+# --------------------------------------------------------------------------
+# invariances and errors
+# --------------------------------------------------------------------------
+
+def _run_decode(qsa, spec, g):
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    kc = torch.zeros((spec.batch, spec.max_blocks(), spec.n_idx_heads, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.compress_keys(d, g["idx_keys"], g["q_pos"], kc, ws)
+    out = torch.empty((spec.batch, spec.n_q, 16, 128), dtype=torch.bfloat16, device="cuda")
+    sp = torch.empty((spec.batch, spec.n_q, 2051), dtype=torch.int32, device="cuda")
+    qsa.decode(d, g["q_idx"], kc, g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"],
+               g["page_table"], g["q_pos"], out, ws, sel_pos=sp)
+    _check_ok(qsa, ws)
+    return out, sp
+
+
+def test_page_permutation_invariance(qsa):
+    spec = small_spec([6000, 3000], n_q=4, seed=31)
+    g = _dev(synth.make_inputs(spec))
+    out0, sp0 = _run_decode(qsa, spec, g)
+    perm = torch.randperm(spec.num_pages(), generator=torch.Generator().manual_seed(3)).cuda()
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(perm.numel(), device="cuda")
+    g2 = dict(g)
+    g2["k_cache"] = g["k_cache"][perm].contiguous()  # new slot i holds old page perm[i]
+    g2["v_cache"] = g["v_cache"][perm].contiguous()
+    pt = g["page_table"].clone()
+    valid = pt >= 0
+    pt[valid] = inv[pt[valid].long()].to(torch.int32)
+    g2["page_table"] = pt
+    out1, sp1 = _run_decode(qsa, spec, g2)
+    assert torch.equal(sp0, sp1)
+    assert torch.equal(out0.view(torch.int16), out1.view(torch.int16))
+
+
+def test_causality_tokens_after_query_do_not_matter(qsa):
+    spec = small_spec([5000], n_q=4, seed=32)
+    g = _dev(synth.make_inputs(spec))
+    out0, sp0 = _run_decode(qsa, spec, g)
+    P = spec.page_size
+    p0 = spec.q_pos()[0][0]
+    g2 = {k: v.clone() for k, v in g.items()}
+    for t in range(p0 + 1, spec.tokens()[0]):
+        page = int(g["page_table"][0, t // P])
+        g2["k_cache"][page, :, t % P] = 3.0
+        g2["v_cache"][page, :, t % P] = -3.0
+    g2["idx_keys"][0, p0 + 1 :] = 5.0
+    out1, sp1 = _run_decode(qsa, spec, g2)
+    assert torch.equal(sp0[0, 0], sp1[0, 0])
+    assert torch.equal(out0[0, 0].view(torch.int16), out1[0, 0].view(torch.int16))
+    assert not torch.equal(out0[0, 3].view(torch.int16), out1[0, 3].view(torch.int16))
+
+
+def test_uniform_v_gives_v(qsa):
+    spec = small_spec([4500], n_q=4, seed=33)
+    g = _dev(synth.make_inputs(spec))
+    row = torch.linspace(-2, 2, 128, device="cuda").to(torch.bfloat16)
+    g["v_cache"][:] = row
+    out, _ = _run_decode(qsa, spec, g)
+    assert torch.max(torch.abs(out.float() - row.float())).item() <= 1e-2
+
+
+def test_device_errors_are_reported_not_fatal(qsa):
+    spec = small_spec([3000, 2000], n_q=2, seed=34)
+    g = _dev(synth.make_inputs(spec))
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    # a query position past the buffers
+    bad = g["q_pos"].clone()
+    bad[1, 1] = 4 * spec.max_blocks() + 100
+    kc = torch.zeros((2, spec.max_blocks(), 1, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((2, 2, 16, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.decode(d, g["q_idx"], kc, g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"],
+               g["page_table"], bad, out, ws)
+    st, info = qsa.check_errors(ws)
+    assert st == qsa.ERR_BAD_INDEX and info[0] == 1 and info[1] == 1 and info[2] == 1
+    assert torch.all(out[1, 1] == 0)
+    assert qsa.check_errors(ws)[0] == qsa.OK  # cleared
+    # a page id outside the cache
+    pt = g["page_table"].clone()
+    pt[0, 3] = spec.num_pages() + 5
+    sel = torch.full((2, 2, 2051), -1, dtype=torch.int32, device="cuda")
+    sel[0, 0, :10] = torch.arange(190, 200, dtype=torch.int32)
+    sel[1, :, 0] = 5
+    qsa.sparse_attn(d, g["q"], g["k_cache"], g["v_cache"], None, None, pt, sel, g["q_pos"], out, ws)
+    st, info = qsa.check_errors(ws)
+    assert st == qsa.ERR_BAD_INDEX and info[0] == 2
+    # a selected position after its query (causality violation)
+    sel2 = sel.clone()
+    sel2[0, 0, :10] = 2999 + 5
+    qsa.sparse_attn(d, g["q"], g["k_cache"], g["v_cache"], None, None, g["page_table"], sel2, g["q_pos"], out, ws)
+    st, info = qsa.check_errors(ws)
+    assert st == qsa.ERR_BAD_INDEX and info[0] == 3 and info[3] == 3004
+    # the context still works afterwards
+    out2, _ = _run_decode(qsa, spec, g)
+    assert torch.isfinite(out2.float()).all()
+
+
+def test_synchronous_argument_errors(qsa):
+    spec = small_spec([3000], n_q=1, seed=35)
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    small = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    f = torch.zeros((1, 1, spec.max_blocks()), device="cuda")
+    qp = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    sb = torch.zeros((1, 1, 512), dtype=torch.int32, device="cuda")
+    sp = torch.zeros((1, 1, 2051), dtype=torch.int32, device="cuda")
+    import ctypes
+
+    st = qsa.lib.qsa_topk(ctypes.byref(d), ctypes.c_void_p(f.data_ptr()), ctypes.c_void_p(qp.data_ptr()),
+                          ctypes.c_void_p(sb.data_ptr()), ctypes.c_void_p(sp.data_ptr()),
+                          ctypes.c_void_p(small.data_ptr()), 256, None)
+    assert st == qsa.ERR_WORKSPACE
+    st = qsa.lib.qsa_topk(ctypes.byref(d), None, ctypes.c_void_p(qp.data_ptr()), ctypes.c_void_p(sb.data_ptr()),
+                          ctypes.c_void_p(sp.data_ptr()), ctypes.c_void_p(ws.data_ptr()), ws.numel(), None)
+    assert st == qsa.ERR_INVALID_ARG
+    d2 = qsa.dims_for_spec(spec)
+    d2.head_dim = 64
+    st = qsa.lib.qsa_topk(ctypes.byref(d2), ctypes.c_void_p(f.data_ptr()), ctypes.c_void_p(qp.data_ptr()),
+                          ctypes.c_void_p(sb.data_ptr()), ctypes.c_void_p(sp.data_ptr()),
+                          ctypes.c_void_p(ws.data_ptr()), ws.numel(), None)
+    assert st == qsa.ERR_UNSUPPORTED
+    with pytest.raises(ValueError):
+        qsa.topk(d, f.cpu(), qp, sb, sp, ws)  # host tensors are refused: no CPU path
