@@ -267,6 +267,7 @@ __global__ void __launch_bounds__(256) score_kernel(const __nv_bfloat16* __restr
           sc_r[(size_t)qsel * max_blocks + b] = tot;
       }
     }
+    u = seg_end;  // the unrolled loop may step past the end of this request's units
   }
   pdl_trigger();
 }
