@@ -271,11 +271,17 @@ def test_sparse_attn_with_holes_and_single_positions(qsa):
 # the fused step, chained stage by stage
 # --------------------------------------------------------------------------
 
-def _near_tie(scores_row, k=512, tol=SCORE_RTOL):
-    if scores_row.shape[0] <= k:
+def _flip_is_near_tie(gpu_blk, ref_blk, ref_scores, k=512, tol=SCORE_RTOL):
+    """True when two selections differ only in blocks whose oracle scores sit
+    within the score tolerance of the oracle's k-th largest score: a boundary
+    that FP32 rounding may legitimately move."""
+    g = set(int(b) for b in gpu_blk if b >= 0)
+    o = set(int(b) for b in ref_blk if b >= 0)
+    if len(g) != len(o):
         return False
-    s = np.sort(scores_row.astype(np.float64))[::-1]
-    return (s[k - 1] - s[k]) <= 2 * tol * max(abs(s[k - 1]), 1.0)
+    thr = np.sort(ref_scores.astype(np.float64))[::-1][k - 1]
+    band = 2 * tol * max(abs(thr), 1.0)
+    return all(abs(float(ref_scores[b]) - thr) <= band for b in g ^ o)
 
 
 def _decode_and_compare(qsa, spec, rows=None, gpu_inputs=None):
@@ -323,10 +329,13 @@ def _decode_and_compare(qsa, spec, rows=None, gpu_inputs=None):
             ref_s = res["scores"][(0, j)]
             got_s = scores[r, j, : ref_s.shape[0]].cpu().numpy().astype(np.float64)
             assert np.max(np.abs(got_s - ref_s) / np.maximum(np.abs(ref_s), 1.0)) <= SCORE_RTOL
-            if _near_tie(ref_s):
+            gsel = sb[r, j].cpu().numpy()
+            if not np.array_equal(gsel, res["sel_blk"][(0, j)]):
+                # allowed only as a near-tie at the selection boundary; then
+                # the two outputs average different sets and are not compared
+                assert _flip_is_near_tie(gsel, res["sel_blk"][(0, j)], ref_s), (r, j)
                 skipped += 1
                 continue
-            assert np.array_equal(sb[r, j].cpu().numpy(), res["sel_blk"][(0, j)]), (r, j)
             assert np.array_equal(sp[r, j].cpu().numpy(), res["sel_pos"][(0, j)]), (r, j)
             err = np.max(np.abs(out[r, j].float().cpu().numpy() - res["out"][(0, j)]))
             assert err <= ATOL[spec.kv_dtype], (r, j, err)
