@@ -31,7 +31,7 @@ BLOCK, TOPK, WIDTH = 4, 512, 2051
 EXPORTS = (
     "qsa_abi_version", "qsa_status_str", "qsa_dims_default", "qsa_workspace_size",
     "qsa_workspace_init", "qsa_compress_keys", "qsa_score", "qsa_topk", "qsa_sparse_attn",
-    "qsa_decode", "qsa_check_errors",
+    "qsa_decode", "qsa_check_errors", "qsa_sparse_attn_noalloc",
 )
 
 
@@ -73,6 +73,7 @@ def _load() -> ctypes.CDLL:
         "qsa_sparse_attn": (I, [D, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "qsa_decode": (I, [D, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "qsa_check_errors": (I, [P, P, ctypes.POINTER(ctypes.c_int32)]),
+        "qsa_sparse_attn_noalloc": (I, [D, P, P, P, P, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -216,6 +217,19 @@ def sparse_attn(d: Dims, q, k_cache, v_cache, k_scale, v_scale, page_table, sel_
     _check(lib.qsa_sparse_attn(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                _ptr(v_scale), _ptr(page_table), _ptr(sel_pos), _ptr(q_pos), _ptr(out), w, n,
                                _stream(stream)), "qsa_sparse_attn")
+
+
+def sparse_attn_noalloc(d: Dims, q, k_cache, v_cache, k_scale, v_scale, page_table, sel_pos, q_pos, out,
+                        stream=None):
+    """sparse_attn without a workspace, for callers that cannot allocate
+    device memory: the library's own static device scratch is used instead.
+    Calls that overlap on the GPU race on that scratch; keep them on one
+    stream."""
+    _check_attn_inputs(d, q, k_cache, v_cache, k_scale, v_scale, page_table, q_pos, out)
+    _want(sel_pos, "sel_pos", (d.batch, d.n_q, d.width), torch.int32)
+    _check(lib.qsa_sparse_attn_noalloc(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                       _ptr(v_scale), _ptr(page_table), _ptr(sel_pos), _ptr(q_pos), _ptr(out),
+                                       _stream(stream)), "qsa_sparse_attn_noalloc")
 
 
 def decode(d: Dims, q_idx, kc, q, k_cache, v_cache, k_scale, v_scale, page_table, q_pos, out, ws,

@@ -1,0 +1,72 @@
+"""qsa_sparse_attn_noalloc: sparse attention for callers that cannot allocate
+device memory (no cudaMalloc allowed where they run, a fixed memory pool, a
+plugin handed tensors but no allocator). It keeps its scratch in the
+library's own static device array instead of a workspace, so the test checks
+that it gives the same output as qsa_sparse_attn, and keeps giving it when
+called again on the array the previous call left behind.
+
+This file is collected last on purpose: a failure here should not stop a run
+before every other test has run.
+"""
+
+import ctypes
+
+import pytest
+import torch
+
+from block_sparse_attention_qsa_gb300 import synth
+from tests._util import small_spec
+
+pytestmark = pytest.mark.gpu
+
+ATOL = {"bf16": 1e-2, "fp8": 3e-2}  # the tolerances of the attention parity tests
+
+
+@pytest.fixture(scope="module")
+def qsa():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    from block_sparse_attention_qsa_gb300 import qsa as q
+
+    return q
+
+
+def _selection(qsa, spec, g, d, ws):
+    kc = torch.zeros((spec.batch, spec.max_blocks(), spec.n_idx_heads, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.compress_keys(d, g["idx_keys"], g["q_pos"], kc, ws)
+    out = torch.empty((spec.batch, spec.n_q, 16, 128), dtype=torch.bfloat16, device="cuda")
+    sel = torch.empty((spec.batch, spec.n_q, 2051), dtype=torch.int32, device="cuda")
+    qsa.decode(d, g["q_idx"], kc, g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"],
+               g["page_table"], g["q_pos"], out, ws, sel_pos=sel)
+    return sel
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_noalloc_matches_workspace_entry_point_on_two_calls(qsa, kv):
+    spec = small_spec([9000, 3001, 2050], n_q=4, kv_dtype=kv, seed=91)
+    g = {k: v.cuda() for k, v in synth.make_inputs(spec).items()}
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    sel = _selection(qsa, spec, g, d, ws)
+    ref = torch.empty((spec.batch, spec.n_q, 16, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.sparse_attn(d, g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"], g["page_table"], sel,
+                    g["q_pos"], ref, ws)
+    st, info = qsa.check_errors(ws)
+    assert st == qsa.OK, info
+    for call in range(2):  # the second call starts from what the first left in the scratch
+        out = torch.full_like(ref, float("nan"))
+        qsa.sparse_attn_noalloc(d, g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"],
+                                g["page_table"], sel, g["q_pos"], out)
+        torch.cuda.synchronize()
+        err = (out.float() - ref.float()).abs().max().item()
+        assert err <= ATOL[kv], (call, err)
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch(qsa):
+    # 300 requests x 4 queries x 2 KV heads = 2,400 split-KV units: too many
+    d = qsa.make_dims(300, 4, 16, 1, 1)
+    fake = ctypes.c_void_p(1 << 20)
+    st = qsa.lib.qsa_sparse_attn_noalloc(ctypes.byref(d), fake, fake, fake, None, None, fake, fake, fake, fake,
+                                         None)
+    assert st == qsa.ERR_WORKSPACE
