@@ -63,7 +63,7 @@ qsa_status check_dims(const qsa_dims* d) {
   if ((long long)d->num_pages * d->n_kv_heads * d->page_size >= (1LL << 31)) return QSA_ERR_UNSUPPORTED;
   if ((long long)d->max_blocks * kBlock >= (1LL << 31)) return QSA_ERR_UNSUPPORTED;
   if ((long long)d->max_pages * d->page_size >= (1LL << 31)) return QSA_ERR_UNSUPPORTED;
-  if ((long long)d->batch * d->n_q * d->n_kv_heads * 64 >= (1LL << 31)) return QSA_ERR_UNSUPPORTED;
+  if ((long long)d->batch * d->n_q * d->n_kv_heads * 128 >= (1LL << 31)) return QSA_ERR_UNSUPPORTED;
   return QSA_OK;
 }
 
@@ -233,7 +233,7 @@ qsa_status qsa_check_errors(void* ws, void* stream, int32_t* info) {
   if (hdr[0] == 0) return QSA_OK;
   if (cudaMemsetAsync(ws, 0, sizeof(hdr), s) != cudaSuccess) return QSA_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return QSA_ERR_CUDA;
-  return QSA_ERR_BAD_INDEX;
+  return hdr[0] == kErrTimeout ? QSA_ERR_TIMEOUT : QSA_ERR_BAD_INDEX;
 }
 
 }  // extern "C"

@@ -20,7 +20,7 @@ constexpr int kGroup = 8;        // query heads per KV head
 constexpr int kMaxNq = 4;        // verify queries per request
 
 // Device error kinds recorded in the workspace header.
-enum DevErr : int32_t { kErrNone = 0, kErrQueryPos = 1, kErrPage = 2, kErrSelPos = 3 };
+enum DevErr : int32_t { kErrNone = 0, kErrQueryPos = 1, kErrPage = 2, kErrSelPos = 3, kErrTimeout = 5 };
 
 // ---------------------------------------------------------------------------
 // Workspace layout (byte offsets from the 256-aligned base).
@@ -40,11 +40,11 @@ struct WsLayout {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Split-KV plan for the attention kernel (shared by sizing and launch).
+// Split-KV plan of the attention kernel (shared by sizing and launch).
 struct AttnPlan {
   int units;            // batch * n_q * n_kv_heads
   int nsplit;           // CTAs per unit
-  int tiles_per_split;  // 64-position tiles per CTA
+  int tiles_per_split;  // 32-position tiles per CTA
 };
 AttnPlan attn_plan(const qsa_dims& d, int num_sms);
 WsLayout ws_layout(const qsa_dims& d, int num_sms);
@@ -67,6 +67,17 @@ __device__ __forceinline__ void record_error(int32_t* hdr, int32_t kind, int32_t
 }
 
 __device__ __forceinline__ int n_full_of(int p) { return (p + 1) >> 2; }
+
+// Order-preserving 32-bit key of a score: a larger score has a larger key;
+// -0.0 maps like +0.0 and NaN below every number. The top 11 bits are the
+// selector's first radix digit.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0u;
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+constexpr int kHistBins = 2048;  // first radix digit: top 11 key bits
 
 // ---------------------------------------------------------------------------
 // host-side launch helper: cudaLaunchKernelEx with optional PDL attribute

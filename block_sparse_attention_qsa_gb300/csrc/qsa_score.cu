@@ -5,16 +5,13 @@
 // scored against each of its (up to 4) verify queries, and the compressed
 // keys are loaded once per request and shared by all queries.
 //
-// GB300 design: the path is a stream over the compressed keys (256 B per
-// block per index head), so the kernel is written for HBM bandwidth, not for
-// tensor cores. Each warp owns a contiguous range of (request, block-pair)
-// units, balanced over the whole batch. A lane loads one 16-byte chunk (8 BF16
-// dims) per block straight into registers with no-L1-allocate 128-bit loads,
-// widens it with shifts (BF16 is the top half of an FP32) and multiplies it
-// against the 4 queries' matching dims with packed FP32 FMAs (FFMA2). The key
-// tile is thereby shared by the 4 queries in registers rather than shared
-// memory. A reduce-scatter butterfly over the lanes of a block then leaves
-// each query's total on its own lanes, so every query costs one shuffle chain.
+// GB300 design: the step streams the compressed keys (256 B per block per
+// index head) once, so the kernel is built for HBM bandwidth. Each warp owns
+// a contiguous, balanced range of 16-block units across the whole batch and
+// keeps several units of 128-bit no-L1-allocate loads in flight. The 4-query
+// contraction runs on the tensor cores (mma.sync, FP32 accumulate) straight
+// from the loaded registers, so the key tile is shared by the 4 queries in
+// registers rather than in shared memory and the ALUs stay idle.
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -88,64 +85,55 @@ __global__ void __launch_bounds__(256) compress_kernel(const uint4* __restrict__
 }
 
 // ---------------------------------------------------------------------------
-// scores
+// scores on tensor cores
+//
+// Per request the scores are the skinny product S[j][b] = sum_k q[j][k] *
+// kc[b][k] over k = (head, dim), with n_q <= 4 queries and thousands of
+// blocks. One warp computes 16 blocks x 8 query columns per mma.sync
+// m16n8k16 (BF16 in, FP32 accumulate; BF16 x BF16 products are exact in
+// FP32): the 16 blocks are the A rows and the queries the B columns (columns
+// n_q..7 are zero). The tensor cores take over the multiply-adds and the
+// cross-lane reduction, so a lane only loads and stores.
+//
+// Fragment layout (lane = 4 * g + c): the lane owns A rows g and g + 8 and,
+// in each 16-wide k step, k columns {2c, 2c+1, 2c+8, 2c+9}; B column g with
+// the same k rows. Since a dot product does not depend on the order of its
+// terms, k is permuted inside each 32-dim chunk so that the lane's 8 dims
+// 8c..8c+7 of the chunk are exactly its k columns of two k steps: one 16-byte
+// load of block row g (and one of row g + 8) fills the A fragments of two
+// mma, and the query chunk at the same dims fills the B fragments.
 // ---------------------------------------------------------------------------
 template <int H>
 struct ScoreGeom {
-  static constexpr int G = (H % 2 == 0) ? 32 : 16;  // lanes covering one block
-  static constexpr int C = H * 16 / G;              // 16-B chunks per lane per block
-  static constexpr int BPW = 32 / G;                // blocks per warp step (a "unit")
-  static constexpr int UNR = 8 / C;                 // units in flight per lane
+  static constexpr int STEPS = 4 * H;             // 32-dim chunks per block row
+  // 16-block units (4 KB per index head) in flight per warp. One 256-thread
+  // CTA per SM with 4 units in flight streams as fast as 4 CTAs with one unit
+  // each, and leaves room on every SM for the selector's CTAs, which then
+  // launch early (programmatic dependent launch) and start the moment the
+  // scores are complete.
+  static constexpr int PD = H == 1 ? 4 : 1;
+  static constexpr int MIN_CTAS = 1;
 };
 
-// Reduce a[0..NQ) over the G lanes of a block; returns the total of query
-// `q` on every lane, and `q` depends on the lane (reduce-scatter).
-template <int G, int NQ>
-__device__ __forceinline__ float reduce_scatter(const float (&a)[NQ], int lane, int& q) {
-  if constexpr (NQ == 4) {
-    constexpr int B1 = G / 2, B2 = G / 4;
-    const bool h1 = lane & B1;
-    float k0 = h1 ? a[2] : a[0], k1 = h1 ? a[3] : a[1];
-    const float s0 = h1 ? a[0] : a[2], s1 = h1 ? a[1] : a[3];
-    k0 += __shfl_xor_sync(kFull, s0, B1);
-    k1 += __shfl_xor_sync(kFull, s1, B1);
-    const bool h2 = lane & B2;
-    float k = h2 ? k1 : k0;
-    const float s = h2 ? k0 : k1;
-    k += __shfl_xor_sync(kFull, s, B2);
-#pragma unroll
-    for (int o = B2 / 2; o >= 1; o >>= 1) k += __shfl_xor_sync(kFull, k, o);
-    q = (h1 ? 2 : 0) + (h2 ? 1 : 0);
-    return k;
-  } else if constexpr (NQ == 2) {
-    constexpr int B1 = G / 2;
-    const bool h1 = lane & B1;
-    float k = h1 ? a[1] : a[0];
-    const float s = h1 ? a[0] : a[1];
-    k += __shfl_xor_sync(kFull, s, B1);
-#pragma unroll
-    for (int o = B1 / 2; o >= 1; o >>= 1) k += __shfl_xor_sync(kFull, k, o);
-    q = h1 ? 1 : 0;
-    return k;
-  } else {
-    float k = a[0];
-#pragma unroll
-    for (int o = G / 2; o >= 1; o >>= 1) k += __shfl_xor_sync(kFull, k, o);
-    q = 0;
-    return k;
-  }
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int H, int NQ>
-__global__ void __launch_bounds__(256) score_kernel(const __nv_bfloat16* __restrict__ q_idx,
+template <int H>
+__global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(const __nv_bfloat16* __restrict__ q_idx,
                                                     const uint4* __restrict__ kc,
                                                     const int32_t* __restrict__ q_pos,
                                                     float* __restrict__ scores, int32_t* err,
                                                     int B, int n_q, int max_blocks) {
   using Geo = ScoreGeom<H>;
-  constexpr int G = Geo::G, C = Geo::C, BPW = Geo::BPW, UNR = Geo::UNR;
-  constexpr int CPB = H * 16;  // 16-B chunks per block
-  extern __shared__ int s_off[];  // [B + 1] first unit of each request
+  constexpr int STEPS = Geo::STEPS, PD = Geo::PD;
+  constexpr int CPB = H * 16;  // 16-B chunks per block row
+  extern __shared__ int s_off[];  // [B + 1] first unit (16 blocks) of each request
 
   pdl_wait();  // no-op unless launched as a dependent
   const int lane = threadIdx.x & 31;
@@ -164,7 +152,7 @@ __global__ void __launch_bounds__(256) score_kernel(const __nv_bfloat16* __restr
             nb = max(nb, n_full_of(p));
           }
         }
-        units = (nb + BPW - 1) / BPW;
+        units = (nb + 15) / 16;
       }
       int v = units;
 #pragma unroll
@@ -185,86 +173,78 @@ __global__ void __launch_bounds__(256) score_kernel(const __nv_bfloat16* __restr
   int u = (int)(U * gw / warps_total);
   const int u_end = (int)(U * (gw + 1) / warps_total);
 
-  // request holding unit u: last r with s_off[r] <= u
-  int lo = 0, hi = B;  // invariant s_off[lo] <= u < s_off[hi] (when u < U)
+  int lo = 0, hi = B;  // last r with s_off[r] <= u
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (s_off[mid] <= u) lo = mid; else hi = mid;
   }
   int r = lo;
-
-  const int slot = (G == 16) ? (lane >> 4) : 0;  // block within the unit
-  int chunk[C];
-#pragma unroll
-  for (int i = 0; i < C; ++i) chunk[i] = (G == 16) ? i * 16 + (lane & 15) : i * 32 + lane;
+  const int g = lane >> 2, c = lane & 3;
 
   while (u < u_end) {
     while (s_off[r + 1] <= u) ++r;
     const int seg_end = min(u_end, s_off[r + 1]);
     const int u0 = s_off[r];
 
-    // this request's queries, widened to FP32 pairs, in the lane's dims
-    float2 qf[NQ][C][4];
-    int nbq[NQ];
+    // B fragments: query g (zero past n_q), dims 8c..8c+7 of every 32-dim chunk
+    uint4 qf[STEPS];
+    int nbq[kMaxNq];
     int nb_r = 0;
 #pragma unroll
-    for (int j = 0; j < NQ; ++j) {
+    for (int j = 0; j < kMaxNq; ++j) {
       int p = -1;
       if (j < n_q) p = q_pos[r * n_q + j];
       const bool ok = p >= 0 && n_full_of(p) <= max_blocks;
       nbq[j] = ok ? n_full_of(p) : 0;
       nb_r = max(nb_r, nbq[j]);
+    }
+    {
+      const uint4* qrow = reinterpret_cast<const uint4*>(q_idx + (size_t)(r * n_q + (g < n_q ? g : 0)) * CPB * 8);
 #pragma unroll
-      for (int i = 0; i < C; ++i) {
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (j < n_q)
-          v = *reinterpret_cast<const uint4*>(q_idx + ((size_t)(r * n_q + j) * CPB + chunk[i]) * 8);
-        qf[j][i][0] = bf16x2_to_f2(v.x);
-        qf[j][i][1] = bf16x2_to_f2(v.y);
-        qf[j][i][2] = bf16x2_to_f2(v.z);
-        qf[j][i][3] = bf16x2_to_f2(v.w);
-      }
+      for (int s = 0; s < STEPS; ++s) qf[s] = (g < n_q) ? qrow[s * 4 + c] : make_uint4(0, 0, 0, 0);
+    }
+    // this lane stores queries 2c, 2c+1 (lanes with c < 2)
+    int nb0 = 0, nb1 = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxNq; ++j) {
+      nb0 = (j == 2 * c) ? nbq[j] : nb0;
+      nb1 = (j == 2 * c + 1) ? nbq[j] : nb1;
     }
     const uint4* kc_r = kc + (size_t)r * max_blocks * CPB;
     float* sc_r = scores + (size_t)r * n_q * max_blocks;
 
-    for (; u < seg_end; u += UNR) {
-      uint4 kv[UNR][C];
+    for (; u < seg_end; u += PD) {
+      uint4 lo_v[PD][STEPS], hi_v[PD][STEPS];
 #pragma unroll
-      for (int k = 0; k < UNR; ++k) {
-        const int b = (u + k - u0) * BPW + slot;
-        const bool ok = (u + k < seg_end) && (b < nb_r);
+      for (int k = 0; k < PD; ++k) {
+        const int b = (u + k - u0) * 16 + g;
+        const bool in = u + k < seg_end;
+        const bool ok0 = in && b < nb_r, ok1 = in && b + 8 < nb_r;
+        const uint4* row0 = kc_r + (size_t)b * CPB + c;
+        const uint4* row1 = row0 + (size_t)8 * CPB;
 #pragma unroll
-        for (int i = 0; i < C; ++i)
-          kv[k][i] = ok ? ld_stream(kc_r + (size_t)b * CPB + chunk[i]) : make_uint4(0, 0, 0, 0);
+        for (int s = 0; s < STEPS; ++s) {
+          lo_v[k][s] = ok0 ? ld_stream(row0 + 4 * s) : make_uint4(0, 0, 0, 0);
+          hi_v[k][s] = ok1 ? ld_stream(row1 + 4 * s) : make_uint4(0, 0, 0, 0);
+        }
       }
 #pragma unroll
-      for (int k = 0; k < UNR; ++k) {
-        float2 acc[NQ];
+      for (int k = 0; k < PD; ++k) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < NQ; ++j) acc[j] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int i = 0; i < C; ++i) {
-          const uint32_t* w = &kv[k][i].x;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 kf = bf16x2_to_f2(w[e]);
-#pragma unroll
-            for (int j = 0; j < NQ; ++j) acc[j] = __ffma2_rn(kf, qf[j][i][e], acc[j]);
-          }
+        for (int s = 0; s < STEPS; ++s) {
+          mma_bf16_16816(acc, lo_v[k][s].x, hi_v[k][s].x, lo_v[k][s].y, hi_v[k][s].y, qf[s].x, qf[s].y);
+          mma_bf16_16816(acc, lo_v[k][s].z, hi_v[k][s].z, lo_v[k][s].w, hi_v[k][s].w, qf[s].z, qf[s].w);
         }
-        float a[NQ];
-#pragma unroll
-        for (int j = 0; j < NQ; ++j) a[j] = acc[j].x + acc[j].y;
-        int qsel;
-        const float tot = reduce_scatter<G, NQ>(a, lane, qsel);
-        const int b = (u + k - u0) * BPW + slot;
-        constexpr int kStoreMask = (NQ == 4) ? (G / 4 - 1) : (NQ == 2 ? (G / 2 - 1) : (G - 1));
-        int nb_sel = 0;
-#pragma unroll
-        for (int j = 0; j < NQ; ++j) nb_sel = (j == qsel) ? nbq[j] : nb_sel;
-        if ((lane & kStoreMask) == 0 && (u + k < seg_end) && b < nb_sel)
-          sc_r[(size_t)qsel * max_blocks + b] = tot;
+        const int b = (u + k - u0) * 16 + g;
+        if (c < 2 && u + k < seg_end) {
+          float* s0 = sc_r + (size_t)(2 * c) * max_blocks;
+          float* s1 = s0 + max_blocks;
+          if (b < nb0) s0[b] = acc[0];
+          if (b < nb1) s1[b] = acc[1];
+          if (b + 8 < nb0) s0[b + 8] = acc[2];
+          if (b + 8 < nb1) s1[b + 8] = acc[3];
+        }
       }
     }
     u = seg_end;  // the unrolled loop may step past the end of this request's units
@@ -272,11 +252,11 @@ __global__ void __launch_bounds__(256) score_kernel(const __nv_bfloat16* __restr
   pdl_trigger();
 }
 
-template <int H, int NQ>
-cudaError_t launch_score_t(const qsa_dims& d, const __nv_bfloat16* q_idx, const __nv_bfloat16* kc,
+template <int H>
+cudaError_t launch_score_h(const qsa_dims& d, const __nv_bfloat16* q_idx, const __nv_bfloat16* kc,
                            const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s,
                            bool pdl) {
-  auto kern = score_kernel<H, NQ>;
+  auto kern = score_kernel<H>;
   const size_t smem = (size_t)(d.batch + 1) * sizeof(int);
   static int occ_cache[64] = {0};
   int dev = 0;
@@ -288,25 +268,14 @@ cudaError_t launch_score_t(const qsa_dims& d, const __nv_bfloat16* q_idx, const 
     if (occ < 1) occ = 1;
     if (dev < 64 && smem <= 48 * 1024) occ_cache[dev] = occ;
   }
-  // upper bound of the work, in units, to avoid launching idle warps
-  using Geo = ScoreGeom<H>;
-  const long long units_ub = (long long)d.batch * ((d.max_blocks + Geo::BPW - 1) / Geo::BPW);
+  // upper bound of the work, in 16-block units, to avoid launching idle warps
+  const long long units_ub = (long long)d.batch * ((d.max_blocks + 15) / 16);
   long long warps = (long long)device_sm_count() * occ * 8;
-  const long long want = (units_ub + 3) / 4;  // at least ~4 units per warp
+  const long long want = (units_ub + 1) / 2;  // at least ~2 units per warp
   if (want < warps) warps = want;
   const int grid = (int)((warps + 7) / 8 > 0 ? (warps + 7) / 8 : 1);
-  return launch_k(kern, dim3(grid), dim3(256), smem, s, pdl, q_idx,
-                  reinterpret_cast<const uint4*>(kc), q_pos, scores, err, d.batch, d.n_q,
-                  d.max_blocks);
-}
-
-template <int H>
-cudaError_t launch_score_h(const qsa_dims& d, const __nv_bfloat16* q_idx, const __nv_bfloat16* kc,
-                           const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s,
-                           bool pdl) {
-  if (d.n_q == 1) return launch_score_t<H, 1>(d, q_idx, kc, q_pos, scores, err, s, pdl);
-  if (d.n_q == 2) return launch_score_t<H, 2>(d, q_idx, kc, q_pos, scores, err, s, pdl);
-  return launch_score_t<H, 4>(d, q_idx, kc, q_pos, scores, err, s, pdl);
+  return launch_k(kern, dim3(grid), dim3(256), smem, s, pdl, q_idx, reinterpret_cast<const uint4*>(kc), q_pos,
+                  scores, err, d.batch, d.n_q, d.max_blocks);
 }
 
 }  // namespace

@@ -7,13 +7,22 @@
 //
 // Design: one 1024-thread CTA per (request, query) row, persistent over rows.
 // Scores map to order-preserving 32-bit keys (-0.0 folded onto +0.0, NaN
-// below everything). Three radix passes of 11, 11 and 10 bits narrow the
-// threshold key T and the number of blocks equal to T still needed; each pass
-// histograms only the keys that match the prefix found so far. The row's keys
-// stay in shared memory when they fit, so the scores are read from HBM once.
-// A final ordered pass keeps every key above T and the lowest-index keys equal
-// to T, and writes block ids and positions in ascending order through
-// ballot/popcount ranks, so the result is deterministic and bit-exact.
+// below everything), so "largest score, lower index on ties" becomes "largest
+// key, lower index on ties". A radix select on the keys finds the threshold
+// key T (the 512th largest) and how many blocks equal to T are still needed.
+//
+// Rows of up to kFastCap blocks whose threshold bin holds at most kCandCap
+// blocks - every 50K-token verify row - take the bitmap path: a first pass
+// (8 loads in flight per thread) histograms the top 11 key bits; a second
+// pass turns each 32 consecutive scores into one word of a "surely selected"
+// bitmap (a higher bin) by warp ballot and appends the threshold bin's blocks
+// to a candidate list; only those candidates - typically a few hundred - go
+// through the two remaining radix passes. Selection is then two bitmaps
+// (surely selected, equal to T) and one block-wide scan over 32-block words
+// writes the block ids and positions in ascending order, the lowest-index
+// ties first. Longer rows, and rows whose threshold bin is crowded, run the
+// radix passes over the whole row (keys cached in shared memory when they
+// fit) and compact in index order tile by tile.
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -21,15 +30,11 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kKeyCap = 53248;  // keys held in shared memory (208 KB)
-constexpr int kHdrWords = 2048 + 64 + 4;
-
-__device__ __forceinline__ uint32_t to_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if ((u & 0x7fffffffu) > 0x7f800000u) return 0u;  // NaN ranks last
-  if (u == 0x80000000u) u = 0u;                      // -0.0 == +0.0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
+constexpr int kFastCap = 24576;  // longest row on the bitmap path (n/32 words <= kThreads)
+constexpr int kKeyCap = 53248;   // keys cached in shared memory on the long-row path
+constexpr int kHdrWords = 2048 + 64 + 8;
+constexpr int kBatch = 8;        // score loads in flight per thread
+constexpr int kCandCap = 8192;   // threshold-bin candidates held on the bitmap path
 
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v, int lane) {
 #pragma unroll
@@ -38,6 +43,21 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v, int lane) {
     if (lane >= o) v += t;
   }
   return v;
+}
+
+// Block-wide exclusive scan of one value per thread; returns the exclusive
+// prefix and writes the total to *total. Uses wsum[0..32); ends with a barrier.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t incl = warp_incl_scan(v, lane);
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) wsum[lane] = warp_incl_scan(wsum[lane], lane);
+  __syncthreads();
+  const uint32_t excl = incl - v + (warp > 0 ? wsum[warp - 1] : 0u);
+  *total = wsum[31];
+  __syncthreads();
+  return excl;
 }
 
 // Finds, scanning bins from the top, the bin d with count(bins > d) < need <=
@@ -76,17 +96,47 @@ __device__ __forceinline__ void find_bin(const uint32_t* hist, uint32_t need, ui
   __syncthreads();
 }
 
+// Reads the row's scores with kBatch loads in flight and calls f(index, key).
+template <typename F>
+__device__ __forceinline__ void for_each_score(const float* srow, int n, F&& f) {
+  for (int base = threadIdx.x; base < n; base += kThreads * kBatch) {
+    float v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * kThreads;
+      v[u] = i < n ? srow[i] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * kThreads;
+      if (i < n) f(i, order_key(v[u]));
+    }
+  }
+}
+
+__device__ __forceinline__ void write_block(int32_t* ob, int32_t* op, uint32_t slot, int b) {
+  if (slot >= (uint32_t)kTopK) return;  // exactly kTopK are selected; the bound is a guard
+  ob[slot] = b;
+  int32_t* o4 = op + kBlock * slot;
+  o4[0] = kBlock * b;
+  o4[1] = kBlock * b + 1;
+  o4[2] = kBlock * b + 2;
+  o4[3] = kBlock * b + 3;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restrict__ scores,
                                                            const int32_t* __restrict__ q_pos,
                                                            int32_t* __restrict__ sel_blk,
                                                            int32_t* __restrict__ sel_pos,
                                                            int32_t* err, int rows, int n_q,
-                                                           int max_blocks, int key_cap) {
+                                                           int max_blocks, int fast_cap, int key_cap) {
   extern __shared__ uint32_t sm[];
-  uint32_t* hist = sm;                                  // [2048]
-  uint32_t* wsum = hist + 2048;                         // [2][32]
-  int* res = reinterpret_cast<int*>(wsum + 64);         // [4]
-  uint32_t* keys = sm + kHdrWords;                      // [key_cap]
+  uint32_t* hist = sm;                           // [2048]
+  uint32_t* wsum = hist + 2048;                  // [2][32]
+  int* res = reinterpret_cast<int*>(wsum + 64);  // [8]
+  // bitmap path: cand_idx[kCandCap], cand_key[kCandCap], 2 bitmaps[fast_cap / 32]
+  // long-row path: keys[key_cap]
+  uint32_t* body = sm + kHdrWords;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
 
@@ -95,96 +145,188 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
     const int p = q_pos[row];
     int32_t* ob = sel_blk + (size_t)row * kTopK;
     int32_t* op = sel_pos + (size_t)row * kWidth;
-    if (p < 0 || n_full_of(p) > max_blocks) {
-      if (tid == 0) record_error(err, kErrQueryPos, row / n_q, row % n_q, p);
-      for (int i = tid; i < kTopK; i += kThreads) ob[i] = -1;
-      for (int i = tid; i < kWidth; i += kThreads) op[i] = -1;
-      continue;
-    }
-    const int n = n_full_of(p);
-    const int npart = (p + 1) & 3;
-    if (n <= kTopK) {  // every full block is kept: positions 0..p
+    const bool p_ok = p >= 0 && n_full_of(p) <= max_blocks;
+    const int n = p_ok ? n_full_of(p) : 0;
+    if (!p_ok || n <= kTopK) {
+      if (!p_ok && tid == 0) record_error(err, kErrQueryPos, row / n_q, row % n_q, p);
+      // every full block is kept (positions 0..p), or nothing for a bad position
       for (int i = tid; i < kTopK; i += kThreads) ob[i] = i < n ? i : -1;
-      for (int i = tid; i < kWidth; i += kThreads) op[i] = i <= p ? i : -1;
+      for (int i = tid; i < kWidth; i += kThreads) op[i] = (p_ok && i <= p) ? i : -1;
       continue;
     }
+    const int npart = (p + 1) & 3;
     const float* srow = scores + (size_t)row * max_blocks;
-    const bool in_smem = n <= key_cap;
 
-    // pass 1: top 11 bits of every key (keys cached in shared memory)
-    for (int i = tid; i < 2048; i += kThreads) hist[i] = 0;
+    // pass 1: histogram of the top 11 key bits
+    const bool in_smem = n > fast_cap && n <= key_cap;  // long rows cache their keys
+    uint32_t* keys = body;
+    for (int i = tid; i < kHistBins; i += kThreads) hist[i] = 0;
     __syncthreads();
-    for (int i = tid; i < n; i += kThreads) {
-      const uint32_t k = to_key(srow[i]);
+    for_each_score(srow, n, [&](int i, uint32_t k) {
       if (in_smem) keys[i] = k;
       atomicAdd(&hist[k >> 21], 1u);
-    }
+    });
     __syncthreads();
     uint32_t need = kTopK;
     find_bin<2048>(hist, need, wsum, res);
-    uint32_t prefix = (uint32_t)res[0];
+    const uint32_t d1 = (uint32_t)res[0];
     need -= (uint32_t)res[1];
+    const uint32_t nb = hist[d1];  // blocks in the threshold bin
 
-    // pass 2: next 11 bits of the keys in the threshold bin
-    for (int i = tid; i < 2048; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < n; i += kThreads) {
-      const uint32_t k = in_smem ? keys[i] : to_key(srow[i]);
-      if ((k >> 21) == prefix) atomicAdd(&hist[(k >> 10) & 2047u], 1u);
-    }
-    __syncthreads();
-    find_bin<2048>(hist, need, wsum, res);
-    prefix = (prefix << 11) | (uint32_t)res[0];
-    need -= (uint32_t)res[1];
-
-    // pass 3: last 10 bits
-    for (int i = tid; i < 1024; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < n; i += kThreads) {
-      const uint32_t k = in_smem ? keys[i] : to_key(srow[i]);
-      if ((k >> 10) == prefix) atomicAdd(&hist[k & 1023u], 1u);
-    }
-    __syncthreads();
-    find_bin<1024>(hist, need, wsum, res);
-    const uint32_t T = (prefix << 10) | (uint32_t)res[0];
-    need -= (uint32_t)res[1];  // blocks equal to T still to take, >= 1
-
-    // ordered compaction: keys > T, then the first `need` keys == T
-    uint32_t n_sel = 0, n_tie = 0;
-    int buf = 0;
-    for (int base = 0; base < n; base += kThreads) {
-      const int i = base + tid;
-      const uint32_t k = (i < n) ? (in_smem ? keys[i] : to_key(srow[i])) : 0u;
-      const bool gt = (i < n) && k > T;
-      const bool eq = (i < n) && k == T;
-      const uint32_t gtm = __ballot_sync(kFull, gt);
-      const uint32_t eqm = __ballot_sync(kFull, eq);
-      uint32_t* wc = wsum + 32 * buf;
-      if (lane == 0) wc[warp] = ((uint32_t)__popc(eqm) << 16) | (uint32_t)__popc(gtm);
+    if (n <= fast_cap && nb <= (uint32_t)kCandCap) {
+      // ---- bitmap path: one pass over the scores, candidates = the threshold bin ----
+      const int nwords = (n + 31) >> 5;
+      uint32_t* cand_idx = body;
+      uint32_t* cand_key = cand_idx + kCandCap;
+      uint32_t* sel_bits = cand_key + kCandCap;       // surely selected, one bit per block
+      uint32_t* tie_bits = sel_bits + fast_cap / 32;  // equal to the threshold
+      if (tid == 0) res[4] = 0;
       __syncthreads();
-      const uint32_t c = wc[lane];
-      const uint32_t incl = warp_incl_scan(c, lane);
-      const uint32_t excl_w = __shfl_sync(kFull, incl - c, warp);
-      const uint32_t total = __shfl_sync(kFull, incl, 31);
-      const uint32_t E_w = excl_w >> 16, G_w = excl_w & 0xffffu;
-      const uint32_t E_t = total >> 16, G_t = total & 0xffffu;
-      const uint32_t rem_tile = need > n_tie ? need - n_tie : 0u;
-      const uint32_t taken_before = min(rem_tile, E_w);
-      const uint32_t rem_w = rem_tile > E_w ? rem_tile - E_w : 0u;
-      const uint32_t my_eq = (uint32_t)__popc(eqm & lt_mask);
-      const bool sel = gt || (eq && my_eq < rem_w);
-      const uint32_t slot = n_sel + G_w + taken_before + (uint32_t)__popc(gtm & lt_mask) + min(my_eq, rem_w);
-      if (sel && slot < (uint32_t)kTopK) {  // exactly kTopK are selected; the bound is a guard
-        ob[slot] = i;
-        int32_t* o4 = op + 4 * slot;
-        o4[0] = 4 * i;
-        o4[1] = 4 * i + 1;
-        o4[2] = 4 * i + 2;
-        o4[3] = 4 * i + 3;
+      for (int w0 = warp; w0 < nwords; w0 += (kThreads / 32) * kBatch) {
+        float v[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int i = ((w0 + u * (kThreads / 32)) << 5) + lane;
+          v[u] = i < n ? srow[i] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int w = w0 + u * (kThreads / 32);
+          if (w >= nwords) break;  // warp-uniform
+          const int i = (w << 5) + lane;
+          const uint32_t k = order_key(v[u]);
+          const uint32_t d = k >> 21;
+          const uint32_t gtm = __ballot_sync(kFull, i < n && d > d1);
+          const uint32_t cm = __ballot_sync(kFull, i < n && d == d1);
+          if (lane == 0) {
+            sel_bits[w] = gtm;
+            tie_bits[w] = 0u;
+          }
+          if (cm) {
+            uint32_t base = 0;
+            if (lane == 0) base = atomicAdd(reinterpret_cast<uint32_t*>(&res[4]), (uint32_t)__popc(cm));
+            base = __shfl_sync(kFull, base, 0);
+            const uint32_t slot = base + (uint32_t)__popc(cm & lt_mask);
+            if ((cm & (1u << lane)) && slot < (uint32_t)kCandCap) {
+              cand_idx[slot] = (uint32_t)i;
+              cand_key[slot] = k;
+            }
+          }
+        }
       }
-      n_sel += G_t + min(rem_tile, E_t);
-      n_tie += E_t;
-      buf ^= 1;
+      for (int i = tid; i < 2048; i += kThreads) hist[i] = 0;
+      __syncthreads();
+      const int nc = min(res[4], kCandCap);
+      // pass 2 over the candidates: key bits 20..10
+      for (int c = tid; c < nc; c += kThreads) atomicAdd(&hist[(cand_key[c] >> 10) & 2047u], 1u);
+      __syncthreads();
+      find_bin<2048>(hist, need, wsum, res);
+      const uint32_t prefix = (d1 << 11) | (uint32_t)res[0];
+      need -= (uint32_t)res[1];
+      for (int i = tid; i < 1024; i += kThreads) hist[i] = 0;
+      __syncthreads();
+      // pass 3: key bits 9..0
+      for (int c = tid; c < nc; c += kThreads) {
+        const uint32_t k = cand_key[c];
+        if ((k >> 10) == prefix) atomicAdd(&hist[k & 1023u], 1u);
+      }
+      __syncthreads();
+      find_bin<1024>(hist, need, wsum, res);
+      const uint32_t T = (prefix << 10) | (uint32_t)res[0];
+      need -= (uint32_t)res[1];  // blocks equal to T still to take, >= 1
+      for (int c = tid; c < nc; c += kThreads) {
+        const uint32_t i = cand_idx[c];
+        const uint32_t k = cand_key[c];
+        if (k > T) atomicOr(&sel_bits[i >> 5], 1u << (i & 31));
+        else if (k == T) atomicOr(&tie_bits[i >> 5], 1u << (i & 31));
+      }
+      __syncthreads();
+      // one word of 32 blocks per thread, in index order
+      uint32_t s = 0, e = 0;
+      if (tid < nwords) {
+        s = sel_bits[tid];
+        e = tie_bits[tid];
+      }
+      uint32_t total;
+      const uint32_t excl = block_excl_scan(((uint32_t)__popc(e) << 16) | (uint32_t)__popc(s), wsum, &total);
+      const uint32_t e_before = excl >> 16, s_before = excl & 0xffffu;
+      const uint32_t taken_before = min(e_before, need);
+      uint32_t take = need > e_before ? min(need - e_before, (uint32_t)__popc(e)) : 0u;
+      uint32_t rest = e;
+      for (uint32_t t = 0; t < take; ++t) rest &= rest - 1u;  // drop the lowest `take` ties
+      uint32_t word = s | (e ^ rest);
+      uint32_t slot = s_before + taken_before;
+      while (word) {
+        const int b = __ffs(word) - 1;
+        write_block(ob, op, slot++, (tid << 5) + b);
+        word &= word - 1u;
+      }
+    } else {
+      // ---- long rows (or a crowded threshold bin): radix passes over the whole row ----
+      __syncthreads();  // every thread has read hist[d1]
+      for (int i = tid; i < 2048; i += kThreads) hist[i] = 0;
+      __syncthreads();
+      auto key_at = [&](int i) { return in_smem ? keys[i] : order_key(srow[i]); };
+      if (in_smem) {
+        for (int i = tid; i < n; i += kThreads) {
+          const uint32_t k = keys[i];
+          if ((k >> 21) == d1) atomicAdd(&hist[(k >> 10) & 2047u], 1u);
+        }
+      } else {
+        for_each_score(srow, n, [&](int, uint32_t k) {
+          if ((k >> 21) == d1) atomicAdd(&hist[(k >> 10) & 2047u], 1u);
+        });
+      }
+      __syncthreads();
+      find_bin<2048>(hist, need, wsum, res);
+      const uint32_t prefix = (d1 << 11) | (uint32_t)res[0];
+      need -= (uint32_t)res[1];
+      for (int i = tid; i < 1024; i += kThreads) hist[i] = 0;
+      __syncthreads();
+      if (in_smem) {
+        for (int i = tid; i < n; i += kThreads) {
+          const uint32_t k = keys[i];
+          if ((k >> 10) == prefix) atomicAdd(&hist[k & 1023u], 1u);
+        }
+      } else {
+        for_each_score(srow, n, [&](int, uint32_t k) {
+          if ((k >> 10) == prefix) atomicAdd(&hist[k & 1023u], 1u);
+        });
+      }
+      __syncthreads();
+      find_bin<1024>(hist, need, wsum, res);
+      const uint32_t T = (prefix << 10) | (uint32_t)res[0];
+      need -= (uint32_t)res[1];
+
+      // ordered compaction: keys > T, then the first `need` keys == T
+      uint32_t n_sel = 0, n_tie = 0;
+      int buf = 0;
+      for (int base = 0; base < n; base += kThreads) {
+        const int i = base + tid;
+        const uint32_t k = (i < n) ? key_at(i) : 0u;
+        const bool gt = (i < n) && k > T;
+        const bool eq = (i < n) && k == T;
+        const uint32_t gtm = __ballot_sync(kFull, gt);
+        const uint32_t eqm = __ballot_sync(kFull, eq);
+        uint32_t* wc = wsum + 32 * buf;
+        if (lane == 0) wc[warp] = ((uint32_t)__popc(eqm) << 16) | (uint32_t)__popc(gtm);
+        __syncthreads();
+        const uint32_t c = wc[lane];
+        const uint32_t incl = warp_incl_scan(c, lane);
+        const uint32_t excl_w = __shfl_sync(kFull, incl - c, warp);
+        const uint32_t total = __shfl_sync(kFull, incl, 31);
+        const uint32_t E_w = excl_w >> 16, G_w = excl_w & 0xffffu;
+        const uint32_t E_t = total >> 16, G_t = total & 0xffffu;
+        const uint32_t rem_tile = need > n_tie ? need - n_tie : 0u;
+        const uint32_t taken_before = min(rem_tile, E_w);
+        const uint32_t rem_w = rem_tile > E_w ? rem_tile - E_w : 0u;
+        const uint32_t my_eq = (uint32_t)__popc(eqm & lt_mask);
+        if (gt || (eq && my_eq < rem_w))
+          write_block(ob, op, n_sel + G_w + taken_before + (uint32_t)__popc(gtm & lt_mask) + min(my_eq, rem_w), i);
+        n_sel += G_t + min(rem_tile, E_t);
+        n_tie += E_t;
+        buf ^= 1;
+      }
     }
     if (tid < kBlock - 1) op[kBlock * kTopK + tid] = tid < npart ? kBlock * n + tid : -1;
     __syncthreads();  // shared memory is reused by the next row
@@ -198,21 +340,28 @@ cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q
                         int32_t* sel_blk, int32_t* sel_pos, int32_t* err, cudaStream_t s,
                         bool pdl) {
   const int rows = d.batch * d.n_q;
-  const int key_cap = d.max_blocks < kKeyCap ? d.max_blocks : kKeyCap;
-  const size_t smem = (size_t)(kHdrWords + key_cap) * sizeof(uint32_t);
+  // shared memory: header + either the bitmap path's candidates and two
+  // bitmaps, or the long-row path's keys
+  const int mb = d.max_blocks;
+  const int mb32 = (mb + 31) / 32 * 32;
+  const int fast_cap = mb <= kTopK ? 0 : (mb32 < kFastCap ? mb32 : kFastCap);
+  const int key_cap = mb > kFastCap ? (mb < kKeyCap ? mb : kKeyCap) : 0;
+  const size_t fast_words = fast_cap ? (size_t)2 * kCandCap + 2 * (fast_cap / 32) : 0;
+  const size_t long_words = (size_t)key_cap;
+  const size_t body = fast_words > long_words ? fast_words : long_words;
+  const size_t smem = (kHdrWords + body) * sizeof(uint32_t);
   static size_t set_bytes[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || set_bytes[dev] < smem) {
-    const size_t want = (size_t)(kHdrWords + kKeyCap) * sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)want);
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    if (dev < 64) set_bytes[dev] = want;
+    if (dev < 64) set_bytes[dev] = smem;
   }
   int grid = rows < device_sm_count() ? rows : device_sm_count();
   if (grid < 1) grid = 1;
   return launch_k(topk_kernel, dim3(grid), dim3(kThreads), smem, s, pdl, scores, q_pos, sel_blk,
-                  sel_pos, err, rows, d.n_q, d.max_blocks, key_cap);
+                  sel_pos, err, rows, d.n_q, d.max_blocks, fast_cap, key_cap);
 }
 
 }  // namespace qsa

@@ -50,6 +50,13 @@ def test_default_dims_are_the_pages_geometry(qsa):
     assert d.kv_dtype == qsa.KV_BF16 and d.sm_scale == 0.0
 
 
+# These pass made-up device pointers, which the calls must refuse before any
+# launch; they run only where no CUDA device exists, so that a regression can
+# only return an error and never touch memory.
+no_device = pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="fake pointers: CPU-only test")
+
+
+@no_device
 def test_workspace_size_and_rejections_need_no_gpu(qsa):
     d = qsa.make_dims(32, 4, 15301, 957, 28352)
     n = ctypes.c_size_t(0)
@@ -85,3 +92,14 @@ def test_binding_refuses_host_tensors(qsa):
     with pytest.raises(ValueError, match="CUDA"):
         qsa.score(d, torch.zeros(1, 1, 1, 128, dtype=torch.bfloat16), torch.zeros(1, 8, 1, 128, dtype=torch.bfloat16),
                   torch.zeros(1, 1, dtype=torch.int32), torch.zeros(1, 1, 8), torch.zeros(4096, dtype=torch.uint8))
+
+
+@no_device
+def test_noalloc_rejects_sizes_beyond_its_scratch(qsa):
+    # 300,000 requests x 4 queries x 2 KV heads: far more split-KV units than
+    # the 8 MiB static scratch holds
+    d = qsa.make_dims(300000, 4, 16, 1, 1)
+    fake = ctypes.c_void_p(1 << 20)
+    st = qsa.lib.qsa_sparse_attn_noalloc(ctypes.byref(d), fake, fake, fake, None, None, fake, fake, fake, fake,
+                                         None)
+    assert st == qsa.ERR_WORKSPACE

@@ -393,6 +393,26 @@ def _run_decode(qsa, spec, g):
     return out, sp
 
 
+def test_decode_repeats_bit_exactly_on_one_workspace(qsa):
+    # the workspace's counters and histograms must be left clean by every call
+    spec = small_spec([9000, 3001, 5000], n_q=4, seed=36)
+    g = _dev(synth.make_inputs(spec))
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    kc = torch.zeros((spec.batch, spec.max_blocks(), 1, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.compress_keys(d, g["idx_keys"], g["q_pos"], kc, ws)
+    outs = []
+    for _ in range(3):
+        out = torch.empty((spec.batch, 4, 16, 128), dtype=torch.bfloat16, device="cuda")
+        sp = torch.empty((spec.batch, 4, 2051), dtype=torch.int32, device="cuda")
+        qsa.decode(d, g["q_idx"], kc, g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"],
+                   g["page_table"], g["q_pos"], out, ws, sel_pos=sp)
+        outs.append((out.view(torch.int16).clone(), sp.clone()))
+    _check_ok(qsa, ws)
+    for o, s in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(s, outs[0][1])
+
+
 def test_page_permutation_invariance(qsa):
     spec = small_spec([6000, 3000], n_q=4, seed=31)
     g = _dev(synth.make_inputs(spec))

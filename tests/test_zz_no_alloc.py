@@ -9,8 +9,6 @@ This file is collected last on purpose: a failure here should not stop a run
 before every other test has run.
 """
 
-import ctypes
-
 import pytest
 import torch
 
@@ -61,12 +59,3 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(qsa, kv):
         torch.cuda.synchronize()
         err = (out.float() - ref.float()).abs().max().item()
         assert err <= ATOL[kv], (call, err)
-
-
-def test_noalloc_rejects_sizes_beyond_its_scratch(qsa):
-    # 300 requests x 4 queries x 2 KV heads = 2,400 split-KV units: too many
-    d = qsa.make_dims(300, 4, 16, 1, 1)
-    fake = ctypes.c_void_p(1 << 20)
-    st = qsa.lib.qsa_sparse_attn_noalloc(ctypes.byref(d), fake, fake, fake, None, None, fake, fake, fake, fake,
-                                         None)
-    assert st == qsa.ERR_WORKSPACE
