@@ -22,19 +22,21 @@ WsLayout ws_layout(const qsa_dims& d, int num_sms) {
   WsLayout w;
   const AttnPlan pl = attn_plan(d, num_sms);
   w.units = pl.units;
-  w.nsplit = pl.nsplit;
-  w.tiles_per_split = pl.tiles_per_split;
+  w.tiles = pl.tiles;
+  w.grid = pl.grid;
   const size_t rows = (size_t)d.batch * d.n_q;
   size_t off = 256;  // header
   w.tickets = off;
   off = align_up(off + (size_t)pl.units * sizeof(int32_t), 256);
   w.partials = off;
-  off = align_up(off + (size_t)pl.units * pl.nsplit * kPartFloats * sizeof(float), 256);
+  off = align_up(off + (size_t)pl.grid * 2 * kPartFloats * sizeof(float), 256);
   w.scores = off;
   off = align_up(off + rows * d.max_blocks * sizeof(float), 256);
   w.sel_blk = off;
   off = align_up(off + rows * kTopK * sizeof(int32_t), 256);
   w.sel_pos = off;
+  off = align_up(off + rows * kWidth * sizeof(int32_t), 256);
+  w.sel_row = off;
   off = align_up(off + rows * kWidth * sizeof(int32_t), 256);
   w.total = off;
   return w;
@@ -169,7 +171,7 @@ qsa_status qsa_topk(const qsa_dims* dims, const float* scores, const int32_t* q_
   if (st != QSA_OK) return st;
   if (!scores || !q_pos || !sel_blk || !sel_pos) return QSA_ERR_INVALID_ARG;
   if ((st = check_ws(dims, ws, ws_bytes, nullptr)) != QSA_OK) return st;
-  return from_cuda(launch_topk(*dims, scores, q_pos, sel_blk, sel_pos, err_word(ws),
+  return from_cuda(launch_topk(*dims, scores, q_pos, sel_blk, sel_pos, err_word(ws), nullptr, nullptr,
                                static_cast<cudaStream_t>(stream), false));
 }
 
@@ -186,11 +188,13 @@ qsa_status qsa_sparse_attn(const qsa_dims* dims, const void* q, const void* k_ca
     return QSA_ERR_INVALID_ARG;
   WsLayout w;
   if ((st = check_ws(dims, ws, ws_bytes, &w)) != QSA_OK) return st;
-  const AttnPlan pl{w.units, w.nsplit, w.tiles_per_split};
-  return from_cuda(launch_attn(*dims, q, k_cache, v_cache, k_scale, v_scale, page_table, sel_pos,
-                               q_pos, out, err_word(ws), at<int32_t>(ws, w.tickets),
-                               at<float>(ws, w.partials), pl, static_cast<cudaStream_t>(stream),
-                               false));
+  const AttnPlan pl{w.units, w.tiles, w.grid};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* srow = at<int32_t>(ws, w.sel_row);
+  if (launch_resolve(*dims, sel_pos, q_pos, page_table, srow, err_word(ws), s) != cudaSuccess)
+    return QSA_ERR_CUDA;
+  return from_cuda(launch_attn(*dims, q, k_cache, v_cache, k_scale, v_scale, srow, out,
+                               at<int32_t>(ws, w.tickets), at<float>(ws, w.partials), pl, s, true));
 }
 
 qsa_status qsa_decode(const qsa_dims* dims, const void* q_idx, const void* kc, const void* q,
@@ -215,11 +219,12 @@ qsa_status qsa_decode(const qsa_dims* dims, const void* q_idx, const void* kc, c
   cudaError_t e = launch_score(*dims, static_cast<const __nv_bfloat16*>(q_idx),
                                static_cast<const __nv_bfloat16*>(kc), q_pos, sc, err_word(ws), s, false);
   if (e != cudaSuccess) return QSA_ERR_CUDA;
-  e = launch_topk(*dims, sc, q_pos, sb, spos, err_word(ws), s, true);
+  int32_t* srow = at<int32_t>(ws, w.sel_row);
+  e = launch_topk(*dims, sc, q_pos, sb, spos, err_word(ws), page_table, srow, s, true);
   if (e != cudaSuccess) return QSA_ERR_CUDA;
-  const AttnPlan pl{w.units, w.nsplit, w.tiles_per_split};
-  e = launch_attn(*dims, q, k_cache, v_cache, k_scale, v_scale, page_table, spos, q_pos, out,
-                  err_word(ws), at<int32_t>(ws, w.tickets), at<float>(ws, w.partials), pl, s, true);
+  const AttnPlan pl{w.units, w.tiles, w.grid};
+  e = launch_attn(*dims, q, k_cache, v_cache, k_scale, v_scale, srow, out, at<int32_t>(ws, w.tickets),
+                  at<float>(ws, w.partials), pl, s, true);
   return from_cuda(e);
 }
 

@@ -56,6 +56,13 @@ __device__ __forceinline__ uint4 ldg16(const void* p) {
   return v;
 }
 
+// a 32-bit load issued at this point of the program (its use may come much later)
+__device__ __forceinline__ int ld_issue(const int32_t* p) {
+  int v;
+  asm volatile("ld.global.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 // 8x8 transpose of 16-bit elements held one pair per lane (lane 4g + c holds
 // row g, columns 2c and 2c+1).
 __device__ __forceinline__ uint32_t movt(uint32_t x) {
@@ -153,315 +160,358 @@ struct AttnArgs {
   const void* v_cache;
   const float* k_scale;
   const float* v_scale;
-  const int32_t* page_table;
-  const int32_t* sel_pos;
-  const int32_t* q_pos;
+  const int32_t* sel_row;  // cache row (KV head 0) of every selected position, -1 for none
   __nv_bfloat16* out;
-  int32_t* err;
   int32_t* tickets;
   float* partials;
-  int n_q, n_kv, page_shift, max_pages, num_pages, width, nsplit, tiles_per_split;
+  long long total;  // units * tiles: the tile stream the CTAs share
+  int tiles, grid, n_kv, page_size, width;
   float sm_scale;
 };
 
-size_t attn_smem_bytes(int tiles_per_split) {
-  // cache rows of the split's positions + warp merge buffer [4][8][128] + stats
-  return (size_t)tiles_per_split * kTile * 4 + 4 * kGroup * kDim * 4 + 512;
+// First tile of CTA c's share of the tile stream, and the CTA holding tile w.
+__device__ __forceinline__ long long tile_begin(const AttnArgs& a, int c) {
+  return (long long)c * a.total / a.grid;
 }
+__device__ __forceinline__ int cta_of_tile(const AttnArgs& a, long long w) {
+  return (int)(((w + 1) * a.grid - 1) / a.total);
+}
+
+// Where the row look-ahead stands: tile t of KV head g of (request, query) row.
+struct Cursor {
+  int t, g, row;
+};
 
 template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const AttnArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  int32_t* s_rows = reinterpret_cast<int32_t*>(smem);                         // [tps * 64]
-  float* wacc = reinterpret_cast<float*>(s_rows + a.tiles_per_split * kTile);  // [4][8][128]
-  float* s_ml = wacc + 4 * kGroup * kDim;                                      // [4][8] m, [4][8] l, M[8], L[8]
+  __shared__ __align__(16) __nv_bfloat16 sQ[2][kGroup * kDim];
+  __shared__ __align__(16) float wacc[4 * kGroup * kDim];  // [warp][head][dim]
+  __shared__ float s_ml[96];
+  __shared__ int s_last;
+
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gq = lane >> 2, c4 = lane & 3;
-  const int unit = blockIdx.x / a.nsplit, split = blockIdx.x % a.nsplit;
-  const int g = unit % a.n_kv, row = unit / a.n_kv;
-  const int r = row / a.n_q;
+  const int ent = warp * kWarpPos + gq;  // this lane's position within a tile
   const int n_q_heads = a.n_kv * kGroup;
-
-  // ---- prologue independent of the previous kernel: Q fragments, scales ----
-  // B fragment of k-step ks for head gq: the lane's pairs 2ks, 2ks + 1 of Q's row
-  uint32_t qb[16];
-  {
-    const __nv_bfloat16* qrow = a.q + ((size_t)row * n_q_heads + g * kGroup + gq) * kDim;
-    if constexpr (FP8) {
-      // dims 16(c + 4i) .. +15 for i = 0, 1 (32 bytes of BF16 each)
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const uint4 lo = *reinterpret_cast<const uint4*>(qrow + 16 * (c4 + 4 * i));
-        const uint4 hi = *reinterpret_cast<const uint4*>(qrow + 16 * (c4 + 4 * i) + 8);
-        qb[8 * i + 0] = bf2_to_h2(lo.x);
-        qb[8 * i + 1] = bf2_to_h2(lo.y);
-        qb[8 * i + 2] = bf2_to_h2(lo.z);
-        qb[8 * i + 3] = bf2_to_h2(lo.w);
-        qb[8 * i + 4] = bf2_to_h2(hi.x);
-        qb[8 * i + 5] = bf2_to_h2(hi.y);
-        qb[8 * i + 6] = bf2_to_h2(hi.z);
-        qb[8 * i + 7] = bf2_to_h2(hi.w);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 v = *reinterpret_cast<const uint4*>(qrow + 8 * (c4 + 4 * i));
-        qb[4 * i + 0] = v.x;
-        qb[4 * i + 1] = v.y;
-        qb[4 * i + 2] = v.z;
-        qb[4 * i + 3] = v.w;
-      }
-    }
-  }
-  const float kscale = FP8 ? a.k_scale[g] : 1.f;
-  const float vscale = FP8 ? a.v_scale[g] : 1.f;
-  const float scale_log2 = a.sm_scale * kscale * kLog2e;
-  const int p = a.q_pos[row];
-  const bool p_ok = p >= 0 && (p >> a.page_shift) < a.max_pages;
-  if (!p_ok && split == 0 && tid == 0 && g == 0) record_error(a.err, kErrQueryPos, r, row % a.n_q, p);
-
-  pdl_wait();  // sel_pos comes from the selection kernel
-
-  // ---- resolve this split's positions to cache rows ----
-  const int pos0 = split * a.tiles_per_split * kTile;
-  const int npos = min(a.tiles_per_split * kTile, a.width - pos0);
-  __shared__ int s_last;
-  if (tid == 0) s_last = -1;
-  __syncthreads();
-  int my_last = -1;
-  const int32_t* sp = a.sel_pos + (size_t)row * a.width + pos0;
-  const int32_t* pt = a.page_table + (size_t)r * a.max_pages;
-  const int page_mask = (1 << a.page_shift) - 1;
-  for (int i = tid; i < a.tiles_per_split * kTile; i += kThreads) {
-    int ri = -1;
-    if (i < npos && p_ok) {
-      const int t = sp[i];
-      if (t > p) {
-        if (g == 0) record_error(a.err, kErrSelPos, r, row % a.n_q, t);
-      } else if (t >= 0) {
-        const int page = pt[t >> a.page_shift];
-        if (page < 0 || page >= a.num_pages) {
-          if (g == 0) record_error(a.err, kErrPage, r, row % a.n_q, page);
-        } else {
-          ri = (page * a.n_kv + g) * (page_mask + 1) + (t & page_mask);
-          my_last = i;
-        }
-      }
-    }
-    s_rows[i] = ri;
-  }
-  if (my_last >= 0) atomicMax(&s_last, my_last);
-  __syncthreads();
-  const int ntiles = (s_last + kTile) / kTile;  // tiles holding a valid position
-
-  // ---- per warp: 8 positions of every tile ----
-  // S^T uses A rows 0..7 (rows 8..15 are zero) and O^T uses k = 0..7 of each
-  // mma: half the tensor work is idle, which costs nothing here, and it halves
-  // the K/V registers so that 16 warps per SM keep gathers in flight.
+  const int P = a.page_size;
   using RR = RowRegs<FP8>;
   const uint8_t* kbase = static_cast<const uint8_t*>(a.k_cache);
   const uint8_t* vbase = static_cast<const uint8_t*>(a.v_cache);
-  float m_run[2] = {kNegInf, kNegInf}, l_run[2] = {0.f, 0.f};  // heads 2c4, 2c4 + 1
-  float acc[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
-  RR kr, vr;  // row gq of the warp's 8 positions
-  int ri = -1;
-  if (ntiles > 0) {
-    ri = s_rows[warp * kWarpPos + gq];
-    kr.load(kbase + (size_t)max(ri, 0) * RR::kRowBytes, c4, ri >= 0);
-    vr.load(vbase + (size_t)max(ri, 0) * RR::kRowBytes, c4, ri >= 0);
+  const int cta = blockIdx.x;
+  const long long w0 = tile_begin(a, cta), w1 = tile_begin(a, cta + 1);
+  if (w0 >= w1) {
+    pdl_trigger();
+    return;
   }
-  for (int t = 0; t < ntiles; ++t) {
-    // S^T (8 positions x 8 heads)
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) mma16816<FP8>(s, kr.pr[2 * ks], 0u, kr.pr[2 * ks + 1], 0u, qb[2 * ks], qb[2 * ks + 1]);
-    const bool ok = ri >= 0;
-    // the next tile's row, and its K loads now that K is consumed
-    int nri = -1;
-    const bool more = t + 1 < ntiles;
-    if (more) {
-      nri = s_rows[(t + 1) * kTile + warp * kWarpPos + gq];
-      kr.load(kbase + (size_t)max(nri, 0) * RR::kRowBytes, c4, nri >= 0);
+  int u = (int)(w0 / a.tiles);
+  int t = (int)(w0 - (long long)u * a.tiles);
+
+  // the 8 query rows of unit uu (2 KB, contiguous) into sQ[buf]
+  auto stage_q = [&](int uu, int buf) {
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(a.q + (size_t)uu * kGroup * kDim) + tid * 16;
+    const uint32_t dst = (uint32_t)__cvta_generic_to_shared(reinterpret_cast<uint8_t*>(sQ[buf]) + tid * 16);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+  };
+  stage_q(u, 0);  // the query is not produced by the previous kernel
+  asm volatile("cp.async.commit_group;" ::: "memory");
+
+  pdl_wait();  // the selection is
+
+  // Row look-ahead: the selection entries of tile w + 2 are loaded while tile w
+  // is processed, and turn into cache rows for the K/V loads of tile w + 1.
+  Cursor L{t, u % a.n_kv, u / a.n_kv};
+  auto load_entry = [&](bool in_range) {
+    const int i = L.t * kTile + ent;
+    return (in_range && i < a.width) ? ld_issue(a.sel_row + (size_t)L.row * a.width + i) : -1;
+  };
+  auto advance = [&]() {
+    if (++L.t == a.tiles) {
+      L.t = 0;
+      if (++L.g == a.n_kv) {
+        L.g = 0;
+        ++L.row;
+      }
     }
-    // online softmax; s[0], s[1]: position gq, heads 2c4, 2c4 + 1
-    const float x0 = ok ? s[0] * scale_log2 : kNegInf;
-    const float x1 = ok ? s[1] * scale_log2 : kNegInf;
-    float mA = x0, mB = x1;
+  };
+  const int e0 = load_entry(true), g0 = L.g;
+  advance();
+  int e1 = load_entry(w0 + 1 < w1), g1 = L.g;
+  advance();
+  long long wl = w0 + 2;  // tile of the cursor
+
+  RR kr, vr;
+  int ri = e0 >= 0 ? e0 + g0 * P : -1;
+  kr.load(kbase + (size_t)max(ri, 0) * RR::kRowBytes, c4, ri >= 0);
+  vr.load(vbase + (size_t)max(ri, 0) * RR::kRowBytes, c4, ri >= 0);
+
+  long long w = w0;
+  for (int buf = 0;; buf ^= 1) {
+    // ---- one segment: tiles [t, t + seg) of unit u ----
+    const int row = u / a.n_kv, g = u - row * a.n_kv;
+    const long long seg_w0 = w;
+    const int seg = (int)min((long long)(a.tiles - t), w1 - w);
+    const bool more = w + seg < w1;  // the share continues with unit u + 1
+    if (more) stage_q(u + 1, buf ^ 1);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 1;" ::: "memory");  // this unit's query has landed
+    __syncthreads();
+
+    uint32_t qb[16];  // B fragments of the KV group's 8 query heads (head gq)
+    {
+      const __nv_bfloat16* qh = sQ[buf] + gq * kDim;
+      if constexpr (FP8) {
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      mA = fmaxf(mA, __shfl_xor_sync(kFull, mA, o));
-      mB = fmaxf(mB, __shfl_xor_sync(kFull, mB, o));
+        for (int i = 0; i < 2; ++i) {
+          const uint4 lo = *reinterpret_cast<const uint4*>(qh + 16 * (c4 + 4 * i));
+          const uint4 hi = *reinterpret_cast<const uint4*>(qh + 16 * (c4 + 4 * i) + 8);
+          const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) qb[8 * i + e] = bf2_to_h2(wd[e]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 v = *reinterpret_cast<const uint4*>(qh + 8 * (c4 + 4 * i));
+          qb[4 * i + 0] = v.x;
+          qb[4 * i + 1] = v.y;
+          qb[4 * i + 2] = v.z;
+          qb[4 * i + 3] = v.w;
+        }
+      }
     }
-    const float nA = fmaxf(m_run[0], mA), nB = fmaxf(m_run[1], mB);
-    const float bA = nA == kNegInf ? 0.f : nA, bB = nB == kNegInf ? 0.f : nB;
-    const float alA = exp2f(m_run[0] - bA), alB = exp2f(m_run[1] - bB);
-    const float p0 = exp2f(x0 - bA), p1 = exp2f(x1 - bB);
-    l_run[0] = l_run[0] * alA + p0;
-    l_run[1] = l_run[1] * alB + p1;
-    m_run[0] = nA;
-    m_run[1] = nB;
+    const float kscale = FP8 ? a.k_scale[g] : 1.f;
+    const float vscale = FP8 ? a.v_scale[g] : 1.f;
+    const float scale_log2 = a.sm_scale * kscale * kLog2e;
+
+    float m_run[2] = {kNegInf, kNegInf}, l_run[2] = {0.f, 0.f};  // heads 2c4, 2c4 + 1
+    float acc[8][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      acc[i][0] *= alA;
-      acc[i][1] *= alB;
-      acc[i][2] *= alA;
-      acc[i][3] *= alB;
-    }
-    // P^T as the B fragment (k = position 0..7, n = head)
-    const uint32_t pb = movt(pack2<FP8>(p0, p1));
-    // O^T (logical dims x heads) += V^T P^T; m-tile mt = logical dims 16mt .. 16mt + 15
+    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+    for (int i = 0; i < seg; ++i, ++w) {
+      // S^T (8 positions x 8 heads)
+      float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-      mma16816<FP8>(acc[mt], movt(vr.pr[2 * mt]), movt(vr.pr[2 * mt + 1]), 0u, 0u, pb, 0u);
-    if (more) {
-      vr.load(vbase + (size_t)max(nri, 0) * RR::kRowBytes, c4, nri >= 0);
+      for (int ks = 0; ks < 8; ++ks) mma16816<FP8>(s, kr.pr[2 * ks], 0u, kr.pr[2 * ks + 1], 0u, qb[2 * ks], qb[2 * ks + 1]);
+      const bool ok = ri >= 0;
+      // the next tile of the share (this unit or the next): its K rows now
+      const bool next = w + 1 < w1;
+      const int nri = e1 >= 0 ? e1 + g1 * P : -1;
+      e1 = load_entry(wl < w1);
+      g1 = L.g;
+      advance();
+      ++wl;
+      if (next) kr.load(kbase + (size_t)max(nri, 0) * RR::kRowBytes, c4, nri >= 0);
+      // online softmax; s[0], s[1]: position gq, heads 2c4, 2c4 + 1
+      const float x0 = ok ? s[0] * scale_log2 : kNegInf;
+      const float x1 = ok ? s[1] * scale_log2 : kNegInf;
+      float mA = x0, mB = x1;
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mA = fmaxf(mA, __shfl_xor_sync(kFull, mA, o));
+        mB = fmaxf(mB, __shfl_xor_sync(kFull, mB, o));
+      }
+      const float nA = fmaxf(m_run[0], mA), nB = fmaxf(m_run[1], mB);
+      const float bA = nA == kNegInf ? 0.f : nA, bB = nB == kNegInf ? 0.f : nB;
+      const float alA = exp2f(m_run[0] - bA), alB = exp2f(m_run[1] - bB);
+      const float p0 = exp2f(x0 - bA), p1 = exp2f(x1 - bB);
+      l_run[0] = l_run[0] * alA + p0;
+      l_run[1] = l_run[1] * alB + p1;
+      m_run[0] = nA;
+      m_run[1] = nB;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        acc[k][0] *= alA;
+        acc[k][1] *= alB;
+        acc[k][2] *= alA;
+        acc[k][3] *= alB;
+      }
+      // O^T += V^T P^T
+      const uint32_t pb = movt(pack2<FP8>(p0, p1));
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+        mma16816<FP8>(acc[mt], movt(vr.pr[2 * mt]), movt(vr.pr[2 * mt + 1]), 0u, 0u, pb, 0u);
+      if (next) vr.load(vbase + (size_t)max(nri, 0) * RR::kRowBytes, c4, nri >= 0);
       ri = nri;
     }
-  }
-  // ---- merge the 4 warps ----
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    l_run[0] += __shfl_xor_sync(kFull, l_run[0], o);
-    l_run[1] += __shfl_xor_sync(kFull, l_run[1], o);
-  }
-  float* cm = s_ml;       // [4][8]
-  float* cl = s_ml + 32;  // [4][8]
-  if (gq == 0) {
-    cm[warp * 8 + 2 * c4] = m_run[0];
-    cm[warp * 8 + 2 * c4 + 1] = m_run[1];
-    cl[warp * 8 + 2 * c4] = l_run[0];
-    cl[warp * 8 + 2 * c4 + 1] = l_run[1];
-  }
-  __syncthreads();
-  float fac[2];
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int h = 2 * c4 + e;
-    float M = kNegInf;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, cm[w * 8 + h]);
-    fac[e] = exp2f(m_run[e] - (M == kNegInf ? 0.f : M));
-  }
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    const int d0 = phys_dim<FP8>(16 * mt + gq), d1 = phys_dim<FP8>(16 * mt + gq + 8);
-    float* w0 = wacc + (warp * 8 + 2 * c4) * kDim;
-    float* w1 = w0 + kDim;
-    w0[d0] = acc[mt][0] * fac[0];
-    w1[d0] = acc[mt][1] * fac[1];
-    w0[d1] = acc[mt][2] * fac[0];
-    w1[d1] = acc[mt][3] * fac[1];
-  }
-  float* sM = s_ml + 64;  // [8]
-  float* sL = s_ml + 72;  // [8]
-  if (tid < 8) {
-    float M = kNegInf;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, cm[w * 8 + tid]);
-    const float Mb = M == kNegInf ? 0.f : M;
-    float L = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) L += cl[w * 8 + tid] * exp2f(cm[w * 8 + tid] - Mb);
-    sM[tid] = M;
-    sL[tid] = L;
-  }
-  __syncthreads();
-  // thread tid owns dim d = tid of all 8 heads
-  float o[8];
-#pragma unroll
-  for (int h = 0; h < 8; ++h)
-    o[h] = wacc[(0 * 8 + h) * kDim + tid] + wacc[(1 * 8 + h) * kDim + tid] +
-           wacc[(2 * 8 + h) * kDim + tid] + wacc[(3 * 8 + h) * kDim + tid];
-  __nv_bfloat16* orow = a.out + ((size_t)row * n_q_heads + g * kGroup) * kDim;
-  if (a.nsplit == 1) {
-#pragma unroll
-    for (int h = 0; h < 8; ++h) {
-      const float l = sL[h];
-      orow[h * kDim + tid] = __float2bfloat16_rn(l > 0.f ? o[h] / l * vscale : 0.f);
-    }
-    pdl_trigger();
-    return;
-  }
 
-  // ---- split-KV: publish the partial, the last arrival merges ----
-  float* part = a.partials + ((size_t)unit * a.nsplit + split) * kPartFloats;
-  if (tid < 8) {
-    part[tid] = sM[tid];
-    part[8 + tid] = sL[tid];
-  }
+    // ---- merge the 4 warps (the next unit's first K/V rows are in flight) ----
 #pragma unroll
-  for (int h = 0; h < 8; ++h) part[16 + h * kDim + tid] = o[h];
-  __threadfence();
-  __syncthreads();
-  __shared__ int s_is_last;
-  if (tid == 0) s_is_last = (atomicAdd(&a.tickets[unit], 1) == a.nsplit - 1);
-  __syncthreads();
-  if (!s_is_last) {
-    pdl_trigger();
-    return;
-  }
-  __threadfence();
-  // every split's (max, sum) at once, then the accumulators 4 splits at a time
-  const float* parts = a.partials + (size_t)unit * a.nsplit * kPartFloats;
-  float* sm_m = wacc;                       // [nsplit][8] (the merge buffer is free now)
-  float* sm_l = wacc + a.nsplit * kGroup;   // [nsplit][8]
-  for (int i = tid; i < a.nsplit * kGroup; i += kThreads) {
-    const int sidx = i >> 3, h = i & 7;
-    sm_m[i] = __ldcg(parts + (size_t)sidx * kPartFloats + h);
-    sm_l[i] = __ldcg(parts + (size_t)sidx * kPartFloats + kGroup + h);
-  }
-  __syncthreads();
-  if (tid < kGroup) {
-    float Ms = kNegInf;
-    for (int sidx = 0; sidx < a.nsplit; ++sidx) Ms = fmaxf(Ms, sm_m[sidx * kGroup + tid]);
-    const float Mbs = (Ms == kNegInf) ? 0.f : Ms;
-    float Ls = 0.f;
-    for (int sidx = 0; sidx < a.nsplit; ++sidx) Ls += sm_l[sidx * kGroup + tid] * exp2f(sm_m[sidx * kGroup + tid] - Mbs);
-    sM[tid] = Mbs;
-    sL[tid] = Ls;
-  }
-  __syncthreads();
+    for (int o = 4; o < 32; o <<= 1) {
+      l_run[0] += __shfl_xor_sync(kFull, l_run[0], o);
+      l_run[1] += __shfl_xor_sync(kFull, l_run[1], o);
+    }
+    float* cm = s_ml;       // [4][8]
+    float* cl = s_ml + 32;  // [4][8]
+    if (gq == 0) {
+      cm[warp * 8 + 2 * c4] = m_run[0];
+      cm[warp * 8 + 2 * c4 + 1] = m_run[1];
+      cl[warp * 8 + 2 * c4] = l_run[0];
+      cl[warp * 8 + 2 * c4 + 1] = l_run[1];
+    }
+    __syncthreads();
+    float fac[2];
 #pragma unroll
-  for (int h = 0; h < 8; ++h) o[h] = 0.f;
-  for (int s0 = 0; s0 < a.nsplit; s0 += 4) {
-    float x[4][8];
+    for (int e = 0; e < 2; ++e) {
+      const int h = 2 * c4 + e;
+      float M = kNegInf;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float* ps = parts + (size_t)(s0 + k) * kPartFloats + 2 * kGroup + tid;
-#pragma unroll
-      for (int h = 0; h < 8; ++h) x[k][h] = (s0 + k < a.nsplit) ? __ldcg(ps + h * kDim) : 0.f;
+      for (int k = 0; k < 4; ++k) M = fmaxf(M, cm[k * 8 + h]);
+      fac[e] = exp2f(m_run[e] - (M == kNegInf ? 0.f : M));
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (s0 + k >= a.nsplit) break;
-#pragma unroll
-      for (int h = 0; h < 8; ++h) o[h] += exp2f(sm_m[(s0 + k) * kGroup + h] - sM[h]) * x[k][h];
+    for (int mt = 0; mt < 8; ++mt) {
+      const int d0 = phys_dim<FP8>(16 * mt + gq), d1 = phys_dim<FP8>(16 * mt + gq + 8);
+      float* r0 = wacc + (warp * 8 + 2 * c4) * kDim;
+      float* r1 = r0 + kDim;
+      r0[d0] = acc[mt][0] * fac[0];
+      r1[d0] = acc[mt][1] * fac[1];
+      r0[d1] = acc[mt][2] * fac[0];
+      r1[d1] = acc[mt][3] * fac[1];
     }
-  }
+    float* sM = s_ml + 64;  // [8]
+    float* sL = s_ml + 72;  // [8]
+    if (tid < 8) {
+      float M = kNegInf;
 #pragma unroll
-  for (int h = 0; h < 8; ++h) {
-    const float l = sL[h];
-    orow[h * kDim + tid] = __float2bfloat16_rn(l > 0.f ? o[h] / l * vscale : 0.f);
+      for (int k = 0; k < 4; ++k) M = fmaxf(M, cm[k * 8 + tid]);
+      const float Mb = M == kNegInf ? 0.f : M;
+      float Ls = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) Ls += cl[k * 8 + tid] * exp2f(cm[k * 8 + tid] - Mb);
+      sM[tid] = M;
+      sL[tid] = Ls;
+    }
+    __syncthreads();
+    // thread tid owns dim tid of all 8 heads
+    float o[8];
+#pragma unroll
+    for (int h = 0; h < 8; ++h)
+      o[h] = wacc[(0 * 8 + h) * kDim + tid] + wacc[(1 * 8 + h) * kDim + tid] +
+             wacc[(2 * 8 + h) * kDim + tid] + wacc[(3 * 8 + h) * kDim + tid];
+    __nv_bfloat16* orow = a.out + ((size_t)row * n_q_heads + g * kGroup) * kDim;
+
+    if (t == 0 && seg == a.tiles) {
+      // the whole unit is in this share: write the output
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        const float l = sL[h];
+        orow[h * kDim + tid] = __float2bfloat16_rn(l > 0.f ? o[h] / l * vscale : 0.f);
+      }
+    } else {
+      // ---- a piece of the unit: publish it, the last piece to arrive merges ----
+      // slot 2c: the share's first segment, 2c + 1: its last (only these two can be pieces)
+      const int slot = 2 * cta + (seg_w0 == w0 ? 0 : 1);
+      float* part = a.partials + (size_t)slot * kPartFloats;
+      if (tid < 8) {
+        part[tid] = sM[tid];
+        part[8 + tid] = sL[tid];
+      }
+#pragma unroll
+      for (int h = 0; h < 8; ++h) part[16 + h * kDim + tid] = o[h];
+      const long long uw0 = (long long)u * a.tiles;
+      const int c_first = cta_of_tile(a, uw0), n_piece = cta_of_tile(a, uw0 + a.tiles - 1) - c_first + 1;
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) s_last = (atomicAdd(&a.tickets[u], 1) == n_piece - 1);
+      __syncthreads();
+      if (s_last) {
+        __threadfence();
+        // every piece's (max, sum) at once, then the accumulators 4 pieces at a time
+        float* pm = wacc;                        // [n_piece][8] (the merge buffer is free now)
+        float* pl = wacc + n_piece * kGroup;     // [n_piece][8]
+        int* ps = reinterpret_cast<int*>(wacc + 2 * n_piece * kGroup);  // [n_piece] slots
+        for (int k = tid; k < n_piece; k += kThreads) {
+          const int cc = c_first + k;
+          ps[k] = 2 * cc + (tile_begin(a, cc) >= uw0 ? 0 : 1);
+        }
+        __syncthreads();
+        for (int i = tid; i < n_piece * kGroup; i += kThreads) {
+          const float* pp = a.partials + (size_t)ps[i >> 3] * kPartFloats;
+          pm[i] = __ldcg(pp + (i & 7));
+          pl[i] = __ldcg(pp + kGroup + (i & 7));
+        }
+        __syncthreads();
+        if (tid < kGroup) {
+          float Ms = kNegInf;
+          for (int k = 0; k < n_piece; ++k) Ms = fmaxf(Ms, pm[k * kGroup + tid]);
+          const float Mbs = (Ms == kNegInf) ? 0.f : Ms;
+          float Ls = 0.f;
+          for (int k = 0; k < n_piece; ++k) Ls += pl[k * kGroup + tid] * exp2f(pm[k * kGroup + tid] - Mbs);
+          sM[tid] = Mbs;
+          sL[tid] = Ls;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int h = 0; h < 8; ++h) o[h] = 0.f;
+        for (int k0 = 0; k0 < n_piece; k0 += 4) {
+          float x[4][8];
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const bool in = k0 + kk < n_piece;
+            const float* pp = a.partials + (size_t)(in ? ps[k0 + kk] : 0) * kPartFloats + 2 * kGroup + tid;
+#pragma unroll
+            for (int h = 0; h < 8; ++h) x[kk][h] = in ? __ldcg(pp + h * kDim) : 0.f;
+          }
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            if (k0 + kk >= n_piece) break;
+#pragma unroll
+            for (int h = 0; h < 8; ++h) o[h] += exp2f(pm[(k0 + kk) * kGroup + h] - sM[h]) * x[kk][h];
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          const float l = sL[h];
+          orow[h * kDim + tid] = __float2bfloat16_rn(l > 0.f ? o[h] / l * vscale : 0.f);
+        }
+        if (tid == 0) a.tickets[u] = 0;  // ready for the next launch
+      }
+    }
+    if (!more) break;
+    ++u;
+    t = 0;
   }
-  if (tid == 0) a.tickets[unit] = 0;
   pdl_trigger();
 }
 
-template <bool FP8>
-cudaError_t launch_attn_t(const AttnArgs& args, int grid, int tiles_per_split, cudaStream_t s, bool pdl) {
-  const size_t smem = attn_smem_bytes(tiles_per_split);
-  static size_t set_bytes[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 64 || set_bytes[dev] < smem) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) set_bytes[dev] = smem;
+// Selected positions -> cache rows of KV head 0 (-1 for none), with the
+// checks of the query position, the selection and the page table.
+__global__ void __launch_bounds__(256) resolve_kernel(const int32_t* __restrict__ sel_pos,
+                                                      const int32_t* __restrict__ q_pos,
+                                                      const int32_t* __restrict__ page_table,
+                                                      int32_t* __restrict__ sel_row, int32_t* err, int n_q,
+                                                      int n_kv, int page_shift, int max_pages, int num_pages,
+                                                      int width) {
+  const int row = blockIdx.x, r = row / n_q, j = row - r * n_q;
+  const int p = q_pos[row];
+  const bool p_ok = p >= 0 && (p >> page_shift) < max_pages;
+  if (!p_ok && threadIdx.x == 0) record_error(err, kErrQueryPos, r, j, p);
+  const int page_mask = (1 << page_shift) - 1;
+  for (int i = threadIdx.x; i < width; i += blockDim.x) {
+    int ri = -1;
+    const int pos = sel_pos[(size_t)row * width + i];
+    if (p_ok && pos >= 0) {
+      if (pos > p) {
+        record_error(err, kErrSelPos, r, j, pos);
+      } else {
+        const int page = page_table[(size_t)r * max_pages + (pos >> page_shift)];
+        if (page < 0 || page >= num_pages)
+          record_error(err, kErrPage, r, j, page);
+        else
+          ri = ((page * n_kv) << page_shift) + (pos & page_mask);
+      }
+    }
+    sel_row[(size_t)row * width + i] = ri;
   }
-  return launch_k(attn_kernel<FP8>, dim3(grid), dim3(kThreads), smem, s, pdl, args);
+  pdl_trigger();
+}
+
+int page_shift_of(int page_size) {
+  int shift = 0;
+  while ((1 << shift) < page_size) ++shift;
+  return shift;
 }
 
 }  // namespace
@@ -469,48 +519,43 @@ cudaError_t launch_attn_t(const AttnArgs& args, int grid, int tiles_per_split, c
 AttnPlan attn_plan(const qsa_dims& d, int num_sms) {
   AttnPlan pl;
   pl.units = d.batch * d.n_q * d.n_kv_heads;
-  const int tiles_total = (d.width + kTile - 1) / kTile;
-  const long long target = 4LL * num_sms * 4;  // ~4 waves of 4 resident CTAs per SM
-  long long ns = (target + pl.units - 1) / pl.units;
-  if (ns < 1) ns = 1;
-  if (ns > tiles_total) ns = tiles_total;
-  pl.tiles_per_split = (tiles_total + (int)ns - 1) / (int)ns;
-  pl.nsplit = (tiles_total + pl.tiles_per_split - 1) / pl.tiles_per_split;
+  pl.tiles = (d.width + kTile - 1) / kTile;
+  const long long total = (long long)pl.units * pl.tiles;
+  const long long resident = 4LL * num_sms;  // 4 CTAs per SM
+  pl.grid = (int)(total < resident ? total : resident);
   return pl;
 }
 
+cudaError_t launch_resolve(const qsa_dims& d, const int32_t* sel_pos, const int32_t* q_pos,
+                           const int32_t* page_table, int32_t* sel_row, int32_t* err, cudaStream_t s) {
+  return launch_k(resolve_kernel, dim3(d.batch * d.n_q), dim3(256), 0, s, false, sel_pos, q_pos, page_table,
+                  sel_row, err, d.n_q, d.n_kv_heads, page_shift_of(d.page_size), d.max_pages, d.num_pages,
+                  d.width);
+}
+
 cudaError_t launch_attn(const qsa_dims& d, const void* q, const void* k_cache, const void* v_cache,
-                        const float* k_scale, const float* v_scale, const int32_t* page_table,
-                        const int32_t* sel_pos, const int32_t* q_pos, void* out, int32_t* err,
-                        int32_t* tickets, float* partials, const AttnPlan& plan, cudaStream_t s,
-                        bool pdl) {
+                        const float* k_scale, const float* v_scale, const int32_t* sel_row, void* out,
+                        int32_t* tickets, float* partials, const AttnPlan& plan, cudaStream_t s, bool pdl) {
   AttnArgs a;
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.k_cache = k_cache;
   a.v_cache = v_cache;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
-  a.page_table = page_table;
-  a.sel_pos = sel_pos;
-  a.q_pos = q_pos;
+  a.sel_row = sel_row;
   a.out = static_cast<__nv_bfloat16*>(out);
-  a.err = err;
   a.tickets = tickets;
   a.partials = partials;
-  a.n_q = d.n_q;
+  a.total = (long long)plan.units * plan.tiles;
+  a.tiles = plan.tiles;
+  a.grid = plan.grid;
   a.n_kv = d.n_kv_heads;
-  int shift = 0;
-  while ((1 << shift) < d.page_size) ++shift;
-  a.page_shift = shift;
-  a.max_pages = d.max_pages;
-  a.num_pages = d.num_pages;
+  a.page_size = d.page_size;
   a.width = d.width;
-  a.nsplit = plan.nsplit;
-  a.tiles_per_split = plan.tiles_per_split;
   a.sm_scale = d.sm_scale > 0.f ? d.sm_scale : 1.0f / sqrtf((float)d.head_dim);
-  const int grid = plan.units * plan.nsplit;
-  if (d.kv_dtype == QSA_KV_FP8_E4M3) return launch_attn_t<true>(a, grid, plan.tiles_per_split, s, pdl);
-  return launch_attn_t<false>(a, grid, plan.tiles_per_split, s, pdl);
+  if (d.kv_dtype == QSA_KV_FP8_E4M3)
+    return launch_k(attn_kernel<true>, dim3(plan.grid), dim3(kThreads), 0, s, pdl, a);
+  return launch_k(attn_kernel<false>, dim3(plan.grid), dim3(kThreads), 0, s, pdl, a);
 }
 
 }  // namespace qsa

@@ -25,26 +25,29 @@ enum DevErr : int32_t { kErrNone = 0, kErrQueryPos = 1, kErrPage = 2, kErrSelPos
 // ---------------------------------------------------------------------------
 // Workspace layout (byte offsets from the 256-aligned base).
 //   [0, 256)           header: int32 err_kind, err_request, err_query, err_value
-//   tickets            int32 [units]           split-KV arrival counters
-//   partials           float [units][nsplit][kPartFloats]
+//   tickets            int32 [units]           arrival counters of split units
+//   partials           float [grid][2][kPartFloats]  pieces of units split between CTAs
 //   scores (decode)    float [B][n_q][max_blocks]
 //   sel_blk (decode)   int32 [B][n_q][512]
 //   sel_pos (decode)   int32 [B][n_q][2051]
+//   sel_row            int32 [B][n_q][2051]    cache row (KV head 0) of each selected position
 // ---------------------------------------------------------------------------
 constexpr int kPartFloats = 2 * kGroup + kGroup * kDim;  // m[8], l[8], acc[8][128]
 
 struct WsLayout {
-  size_t tickets, partials, scores, sel_blk, sel_pos, total;
-  int units, nsplit, tiles_per_split;
+  size_t tickets, partials, scores, sel_blk, sel_pos, sel_row, total;
+  int units, tiles, grid;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Split-KV plan of the attention kernel (shared by sizing and launch).
+// Work plan of the attention kernel (shared by sizing and launch): the
+// units * tiles 32-position tiles form one stream, cut into `grid` contiguous
+// shares of equal length, one per CTA.
 struct AttnPlan {
-  int units;            // batch * n_q * n_kv_heads
-  int nsplit;           // CTAs per unit
-  int tiles_per_split;  // 32-position tiles per CTA
+  int units;  // batch * n_q * n_kv_heads
+  int tiles;  // 32-position tiles per unit
+  int grid;   // CTAs
 };
 AttnPlan attn_plan(const qsa_dims& d, int num_sms);
 WsLayout ws_layout(const qsa_dims& d, int num_sms);
@@ -106,12 +109,16 @@ cudaError_t launch_compress(const qsa_dims& d, const __nv_bfloat16* idx_keys, co
                             cudaStream_t s);
 cudaError_t launch_score(const qsa_dims& d, const __nv_bfloat16* q_idx, const __nv_bfloat16* kc,
                          const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s, bool pdl);
+// page_table / sel_row (optional, inside qsa_decode): also write each selected
+// position's cache row for KV head 0, so attention skips the page lookup
 cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q_pos,
-                        int32_t* sel_blk, int32_t* sel_pos, int32_t* err, cudaStream_t s, bool pdl);
+                        int32_t* sel_blk, int32_t* sel_pos, int32_t* err, const int32_t* page_table,
+                        int32_t* sel_row, cudaStream_t s, bool pdl);
+// selected positions -> cache rows (KV head 0) with all index checks
+cudaError_t launch_resolve(const qsa_dims& d, const int32_t* sel_pos, const int32_t* q_pos,
+                           const int32_t* page_table, int32_t* sel_row, int32_t* err, cudaStream_t s);
 cudaError_t launch_attn(const qsa_dims& d, const void* q, const void* k_cache, const void* v_cache,
-                        const float* k_scale, const float* v_scale, const int32_t* page_table,
-                        const int32_t* sel_pos, const int32_t* q_pos, void* out, int32_t* err,
-                        int32_t* tickets, float* partials, const AttnPlan& plan, cudaStream_t s,
-                        bool pdl);
+                        const float* k_scale, const float* v_scale, const int32_t* sel_row, void* out,
+                        int32_t* tickets, float* partials, const AttnPlan& plan, cudaStream_t s, bool pdl);
 
 }  // namespace qsa

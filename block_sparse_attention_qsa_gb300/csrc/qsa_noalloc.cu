@@ -1,7 +1,8 @@
 // Sparse attention for callers that cannot allocate device memory.
 //
-// qsa_sparse_attn keeps its split-KV scratch (arrival tickets and per-split
-// softmax partials) in a caller-provided workspace. Some callers cannot make
+// qsa_sparse_attn keeps its scratch (the resolved cache rows, arrival tickets
+// and the softmax partials of units split between CTAs) in a caller-provided
+// workspace. Some callers cannot make
 // that allocation: code that runs where cudaMalloc is forbidden or unsafe
 // (inside a custom allocator's own callbacks, in a process whose memory pool
 // is fixed up front, in plugins that are handed tensors but no allocator).
@@ -15,10 +16,10 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(8) << 20;  // 8 MiB per device
-constexpr size_t kHeaderBytes = 256;                // device error record
+constexpr size_t kScratchBytes = size_t(16) << 20;  // 16 MiB per device
+constexpr size_t kHeaderBytes = 256;                 // device error record
 
-// [header][tickets, 256-aligned][split partials]
+// [header][tickets][cache rows][partials], each part 256-aligned
 static __device__ __align__(256) unsigned char g_attn_scratch[kScratchBytes];
 
 // Device addresses of g_attn_scratch, one per device, found once. In host
@@ -58,30 +59,30 @@ extern "C" qsa_status qsa_sparse_attn_noalloc(const qsa_dims* dims, const void* 
       (reinterpret_cast<uintptr_t>(q) & 3u))
     return QSA_ERR_INVALID_ARG;
 
-  // The usual split plan, with fewer splits if its partials would not fit.
+  // The usual plan, with fewer CTAs (so fewer partials) if it would not fit.
   qsa::AttnPlan plan = qsa::attn_plan(*dims, qsa::device_sm_count());
+  const size_t rows = (size_t)dims->batch * dims->n_q;
   const size_t ticket_bytes = qsa::align_up((size_t)plan.units * sizeof(int32_t), 256);
-  const size_t part_bytes = (size_t)qsa::kPartFloats * sizeof(float);
-  if (kHeaderBytes + ticket_bytes >= kScratchBytes) return QSA_ERR_WORKSPACE;
-  const size_t room = kScratchBytes - kHeaderBytes - ticket_bytes;
-  const size_t max_split = room / (part_bytes * (size_t)plan.units);
-  if (max_split < 1) return QSA_ERR_WORKSPACE;  // even one split per unit is too large
-  if ((size_t)plan.nsplit > max_split) {
-    const int covered = plan.nsplit * plan.tiles_per_split;  // tiles the plan spans
-    plan.nsplit = (int)max_split;
-    plan.tiles_per_split = (covered + plan.nsplit - 1) / plan.nsplit;
-  }
+  const size_t row_bytes = qsa::align_up(rows * dims->width * sizeof(int32_t), 256);
+  const size_t piece_bytes = 2 * (size_t)qsa::kPartFloats * sizeof(float);  // two per CTA
+  const size_t fixed = kHeaderBytes + ticket_bytes + row_bytes;
+  if (fixed + piece_bytes > kScratchBytes) return QSA_ERR_WORKSPACE;  // not even one CTA fits
+  const size_t max_grid = (kScratchBytes - fixed) / piece_bytes;
+  if ((size_t)plan.grid > max_grid) plan.grid = (int)max_grid;
 
   void* scratch = nullptr;
   const qsa_status ss = scratch_on_current_device(&scratch);
   if (ss != QSA_OK) return ss;
   unsigned char* base = static_cast<unsigned char*>(scratch);
+  int32_t* err = reinterpret_cast<int32_t*>(base);
+  int32_t* tickets = reinterpret_cast<int32_t*>(base + kHeaderBytes);
+  int32_t* sel_row = reinterpret_cast<int32_t*>(base + kHeaderBytes + ticket_bytes);
+  float* partials = reinterpret_cast<float*>(base + fixed);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the error record and the arrival tickets must start at zero every call
   if (cudaMemsetAsync(base, 0, kHeaderBytes + ticket_bytes, s) != cudaSuccess) return QSA_ERR_CUDA;
-  const cudaError_t e = qsa::launch_attn(
-      *dims, q, k_cache, v_cache, k_scale, v_scale, page_table, sel_pos, q_pos, out,
-      reinterpret_cast<int32_t*>(base), reinterpret_cast<int32_t*>(base + kHeaderBytes),
-      reinterpret_cast<float*>(base + kHeaderBytes + ticket_bytes), plan, s, false);
+  if (qsa::launch_resolve(*dims, sel_pos, q_pos, page_table, sel_row, err, s) != cudaSuccess) return QSA_ERR_CUDA;
+  const cudaError_t e = qsa::launch_attn(*dims, q, k_cache, v_cache, k_scale, v_scale, sel_row, out, tickets,
+                                         partials, plan, s, true);
   return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA;
 }

@@ -114,7 +114,26 @@ __device__ __forceinline__ void for_each_score(const float* srow, int n, F&& f) 
   }
 }
 
-__device__ __forceinline__ void write_block(int32_t* ob, int32_t* op, uint32_t slot, int b) {
+// Optional output inside qsa_decode: the cache row (for KV head 0) of every
+// selected position, so the attention kernel needs no page lookup.
+struct RowOut {
+  const int32_t* page_table;  // [B][max_pages], or null: no rows written
+  int32_t* sel_row;           // [rows][kWidth]
+  int max_pages, num_pages, page_shift, n_kv;
+};
+
+// cache row of position pos of request r (KV head 0), or -1 for a bad page
+__device__ __forceinline__ int row_of(const RowOut& ro, int r, int pos, int32_t* err, int j) {
+  const int page = ro.page_table[(size_t)r * ro.max_pages + (pos >> ro.page_shift)];
+  if (page < 0 || page >= ro.num_pages) {
+    record_error(err, kErrPage, r, j, page);
+    return -1;
+  }
+  return (page * ro.n_kv << ro.page_shift) + (pos & ((1 << ro.page_shift) - 1));
+}
+
+__device__ __forceinline__ void write_block(int32_t* ob, int32_t* op, int32_t* orow, const RowOut& ro,
+                                            int32_t* err, int r, int j, uint32_t slot, int b) {
   if (slot >= (uint32_t)kTopK) return;  // exactly kTopK are selected; the bound is a guard
   ob[slot] = b;
   int32_t* o4 = op + kBlock * slot;
@@ -122,14 +141,23 @@ __device__ __forceinline__ void write_block(int32_t* ob, int32_t* op, uint32_t s
   o4[1] = kBlock * b + 1;
   o4[2] = kBlock * b + 2;
   o4[3] = kBlock * b + 3;
+  if (orow) {
+    const int base = row_of(ro, r, kBlock * b, err, j);  // a block never straddles a page
+    int32_t* w4 = orow + kBlock * slot;
+    w4[0] = base;
+    w4[1] = base < 0 ? -1 : base + 1;
+    w4[2] = base < 0 ? -1 : base + 2;
+    w4[3] = base < 0 ? -1 : base + 3;
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restrict__ scores,
                                                            const int32_t* __restrict__ q_pos,
                                                            int32_t* __restrict__ sel_blk,
                                                            int32_t* __restrict__ sel_pos,
-                                                           int32_t* err, int rows, int n_q,
-                                                           int max_blocks, int fast_cap, int key_cap) {
+                                                           int32_t* err, const RowOut ro, int rows,
+                                                           int n_q, int max_blocks, int fast_cap,
+                                                           int key_cap) {
   extern __shared__ uint32_t sm[];
   uint32_t* hist = sm;                           // [2048]
   uint32_t* wsum = hist + 2048;                  // [2][32]
@@ -145,13 +173,17 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
     const int p = q_pos[row];
     int32_t* ob = sel_blk + (size_t)row * kTopK;
     int32_t* op = sel_pos + (size_t)row * kWidth;
-    const bool p_ok = p >= 0 && n_full_of(p) <= max_blocks;
+    int32_t* orow = ro.page_table ? ro.sel_row + (size_t)row * kWidth : nullptr;
+    const int r = row / n_q, j = row - r * n_q;
+    const bool p_ok = p >= 0 && n_full_of(p) <= max_blocks && (!orow || (p >> ro.page_shift) < ro.max_pages);
     const int n = p_ok ? n_full_of(p) : 0;
     if (!p_ok || n <= kTopK) {
-      if (!p_ok && tid == 0) record_error(err, kErrQueryPos, row / n_q, row % n_q, p);
+      if (!p_ok && tid == 0) record_error(err, kErrQueryPos, r, j, p);
       // every full block is kept (positions 0..p), or nothing for a bad position
       for (int i = tid; i < kTopK; i += kThreads) ob[i] = i < n ? i : -1;
       for (int i = tid; i < kWidth; i += kThreads) op[i] = (p_ok && i <= p) ? i : -1;
+      if (orow)
+        for (int i = tid; i < kWidth; i += kThreads) orow[i] = (p_ok && i <= p) ? row_of(ro, r, i, err, j) : -1;
       continue;
     }
     const int npart = (p + 1) & 3;
@@ -258,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
       uint32_t slot = s_before + taken_before;
       while (word) {
         const int b = __ffs(word) - 1;
-        write_block(ob, op, slot++, (tid << 5) + b);
+        write_block(ob, op, orow, ro, err, r, j, slot++, (tid << 5) + b);
         word &= word - 1u;
       }
     } else {
@@ -322,13 +354,17 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
         const uint32_t rem_w = rem_tile > E_w ? rem_tile - E_w : 0u;
         const uint32_t my_eq = (uint32_t)__popc(eqm & lt_mask);
         if (gt || (eq && my_eq < rem_w))
-          write_block(ob, op, n_sel + G_w + taken_before + (uint32_t)__popc(gtm & lt_mask) + min(my_eq, rem_w), i);
+          write_block(ob, op, orow, ro, err, r, j,
+                      n_sel + G_w + taken_before + (uint32_t)__popc(gtm & lt_mask) + min(my_eq, rem_w), i);
         n_sel += G_t + min(rem_tile, E_t);
         n_tie += E_t;
         buf ^= 1;
       }
     }
-    if (tid < kBlock - 1) op[kBlock * kTopK + tid] = tid < npart ? kBlock * n + tid : -1;
+    if (tid < kBlock - 1) {
+      op[kBlock * kTopK + tid] = tid < npart ? kBlock * n + tid : -1;
+      if (orow) orow[kBlock * kTopK + tid] = tid < npart ? row_of(ro, r, kBlock * n + tid, err, j) : -1;
+    }
     __syncthreads();  // shared memory is reused by the next row
   }
   pdl_trigger();
@@ -337,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
 }  // namespace
 
 cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q_pos,
-                        int32_t* sel_blk, int32_t* sel_pos, int32_t* err, cudaStream_t s,
-                        bool pdl) {
+                        int32_t* sel_blk, int32_t* sel_pos, int32_t* err, const int32_t* page_table,
+                        int32_t* sel_row, cudaStream_t s, bool pdl) {
   const int rows = d.batch * d.n_q;
   // shared memory: header + either the bitmap path's candidates and two
   // bitmaps, or the long-row path's keys
@@ -360,8 +396,17 @@ cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q
   }
   int grid = rows < device_sm_count() ? rows : device_sm_count();
   if (grid < 1) grid = 1;
+  RowOut ro;
+  ro.page_table = page_table;
+  ro.sel_row = sel_row;
+  ro.max_pages = d.max_pages;
+  ro.num_pages = d.num_pages;
+  int shift = 0;
+  while ((1 << shift) < d.page_size) ++shift;
+  ro.page_shift = shift;
+  ro.n_kv = d.n_kv_heads;
   return launch_k(topk_kernel, dim3(grid), dim3(kThreads), smem, s, pdl, scores, q_pos, sel_blk,
-                  sel_pos, err, rows, d.n_q, d.max_blocks, fast_cap, key_cap);
+                  sel_pos, err, ro, rows, d.n_q, d.max_blocks, fast_cap, key_cap);
 }
 
 }  // namespace qsa

@@ -187,19 +187,19 @@ qsa_status qsa_decode(const qsa_dims* dims, const void* q_idx, const void* kc, c
  * where cudaMalloc is not allowed, a process whose memory pool is fixed up
  * front, a plugin handed tensors but no allocator). The pages have no
  * counterpart: it is a deployment convenience of this library. Same inputs,
- * output and arithmetic as qsa_sparse_attn, but no workspace argument: the
- * split-KV scratch lives in an 8 MiB array in the library's own device image,
- * which every GPU that loads the library keeps until the process exits.
+ * output and arithmetic as qsa_sparse_attn, but no workspace argument: its
+ * scratch (resolved cache rows, arrival tickets, softmax partials) lives in a
+ * 16 MiB array in the library's own device image, which every GPU that loads
+ * the library keeps until the process exits.
  * The call allocates nothing (no cudaMalloc, no cudaFree, no allocating
  * library routine). The first call on a device looks up that array's device
  * address (cudaGetSymbolAddress) with the device current, so make it before
  * any stream capture. Every call shares the one array per device and clears
  * its counters at the start, so calls that overlap on the GPU (different
  * streams, or different host threads on one device) race: issue them in
- * order on one stream. The split count is lowered to fit the array; when
- * even one split per (request, query, KV head) does not fit, that is
- * batch * n_q * n_kv_heads above about 2,000, the call returns
- * QSA_ERR_WORKSPACE before launching anything. Device-side index errors are
+ * order on one stream. The CTA count is lowered to fit the array; when even
+ * one CTA does not fit, that is batch * n_q above about 2,040 at 2 KV heads,
+ * the call returns QSA_ERR_WORKSPACE before launching anything. Device-side index errors are
  * skipped as in qsa_sparse_attn, but there is no workspace to read them back
  * from: use qsa_sparse_attn to diagnose them. */
 qsa_status qsa_sparse_attn_noalloc(const qsa_dims* dims, const void* q, const void* k_cache,
