@@ -11,18 +11,21 @@
 // key, lower index on ties". A radix select on the keys finds the threshold
 // key T (the 512th largest) and how many blocks equal to T are still needed.
 //
-// Rows of up to kFastCap blocks whose threshold bin holds at most kCandCap
-// blocks - every 50K-token verify row - take the bitmap path: a first pass
-// (8 loads in flight per thread) histograms the top 11 key bits; a second
-// pass turns each 32 consecutive scores into one word of a "surely selected"
-// bitmap (a higher bin) by warp ballot and appends the threshold bin's blocks
-// to a candidate list; only those candidates - typically a few hundred - go
-// through the two remaining radix passes. Selection is then two bitmaps
-// (surely selected, equal to T) and one block-wide scan over 32-block words
-// writes the block ids and positions in ascending order, the lowest-index
-// ties first. Longer rows, and rows whose threshold bin is crowded, run the
+// Rows of up to kFastCap blocks - every 50K-token verify row - take the
+// register path: thread t loads the scores of a contiguous run of at most
+// kKpt blocks (16-byte loads when the buffer allows) and keeps their keys in
+// registers. Pass 1 histograms the top 11 key bits; pass 2 classifies each
+// key against the threshold bin into two register bit masks (above it, in
+// it) and histograms the next 11 bits of the keys in it; a third digit is
+// needed only when digit 2's bin is not taken whole. Because thread order is
+// index order, one block-wide scan of the per-thread counts then lists the
+// selected blocks ascending, the lowest-index ties first, and all threads
+// write the outputs from that list with coalesced stores. Longer rows run the
 // radix passes over the whole row (keys cached in shared memory when they
-// fit) and compact in index order tile by tile.
+// fit) and list the selection in index order tile by tile. The request's
+// page table is staged in shared memory (before waiting on the score kernel,
+// for a CTA's first row) so the cache rows written inside qsa_decode need no
+// dependent global loads.
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -30,11 +33,13 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kFastCap = 24576;  // longest row on the bitmap path (n/32 words <= kThreads)
-constexpr int kKeyCap = 53248;   // keys cached in shared memory on the long-row path
-constexpr int kHdrWords = 2048 + 64 + 8;
-constexpr int kBatch = 8;        // score loads in flight per thread
-constexpr int kCandCap = 8192;   // threshold-bin candidates held on the bitmap path
+constexpr int kKpt = 24;         // keys per thread on the register path
+constexpr int kFastCap = kKpt * kThreads - 4;  // longest row on it (3 blocks of alignment slack)
+constexpr int kKeyCap = 49152;   // keys cached in shared memory on the long-row path
+constexpr int kPtCap = 4096;     // page-table entries staged in shared memory
+// header: hist[2048], hist2[2048], wsum[64], res[8], blk[512], pt[kPtCap]
+constexpr int kHdrWords = 2048 + 2048 + 64 + 8 + kTopK + kPtCap;
+constexpr int kBatch = 8;        // score loads in flight per thread (long-row path)
 
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v, int lane) {
 #pragma unroll
@@ -96,20 +101,23 @@ __device__ __forceinline__ void find_bin(const uint32_t* hist, uint32_t need, ui
   __syncthreads();
 }
 
-// Reads the row's scores with kBatch loads in flight and calls f(index, key).
+// Reads the row's scores with kBatch loads in flight and calls f(index,
+// valid, key) on all lanes of a warp together (index >= n: valid false).
 template <typename F>
 __device__ __forceinline__ void for_each_score(const float* srow, int n, F&& f) {
-  for (int base = threadIdx.x; base < n; base += kThreads * kBatch) {
+  const int lane = threadIdx.x & 31;
+  for (int wb = threadIdx.x & ~31; wb < n; wb += kThreads * kBatch) {  // warp-uniform
     float v[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
-      const int i = base + u * kThreads;
+      const int i = wb + lane + u * kThreads;
       v[u] = i < n ? srow[i] : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
-      const int i = base + u * kThreads;
-      if (i < n) f(i, order_key(v[u]));
+      if (wb + u * kThreads >= n) break;  // warp-uniform
+      const int i = wb + lane + u * kThreads;
+      f(i, i < n, order_key(v[u]));
     }
   }
 }
@@ -122,9 +130,11 @@ struct RowOut {
   int max_pages, num_pages, page_shift, n_kv;
 };
 
-// cache row of position pos of request r (KV head 0), or -1 for a bad page
-__device__ __forceinline__ int row_of(const RowOut& ro, int r, int pos, int32_t* err, int j) {
-  const int page = ro.page_table[(size_t)r * ro.max_pages + (pos >> ro.page_shift)];
+// cache row of position pos of request r (KV head 0), or -1 for a bad page;
+// pt: the request's page table staged in shared memory, or null
+__device__ __forceinline__ int row_of(const RowOut& ro, const int32_t* pt, int r, int pos, int32_t* err, int j) {
+  const int pi = pos >> ro.page_shift;
+  const int page = pt ? pt[pi] : ro.page_table[(size_t)r * ro.max_pages + pi];
   if (page < 0 || page >= ro.num_pages) {
     record_error(err, kErrPage, r, j, page);
     return -1;
@@ -132,23 +142,10 @@ __device__ __forceinline__ int row_of(const RowOut& ro, int r, int pos, int32_t*
   return (page * ro.n_kv << ro.page_shift) + (pos & ((1 << ro.page_shift) - 1));
 }
 
-__device__ __forceinline__ void write_block(int32_t* ob, int32_t* op, int32_t* orow, const RowOut& ro,
-                                            int32_t* err, int r, int j, uint32_t slot, int b) {
-  if (slot >= (uint32_t)kTopK) return;  // exactly kTopK are selected; the bound is a guard
-  ob[slot] = b;
-  int32_t* o4 = op + kBlock * slot;
-  o4[0] = kBlock * b;
-  o4[1] = kBlock * b + 1;
-  o4[2] = kBlock * b + 2;
-  o4[3] = kBlock * b + 3;
-  if (orow) {
-    const int base = row_of(ro, r, kBlock * b, err, j);  // a block never straddles a page
-    int32_t* w4 = orow + kBlock * slot;
-    w4[0] = base;
-    w4[1] = base < 0 ? -1 : base + 1;
-    w4[2] = base < 0 ? -1 : base + 2;
-    w4[3] = base < 0 ? -1 : base + 3;
-  }
+// histogram update (plain shared-memory atomics: measured on GB300, grouping
+// equal bins of a warp with match.any first costs several times more)
+__device__ __forceinline__ void hist_add(uint32_t* hist, bool valid, uint32_t bin, int) {
+  if (valid) atomicAdd(&hist[bin], 1u);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restrict__ scores,
@@ -157,23 +154,46 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
                                                            int32_t* __restrict__ sel_pos,
                                                            int32_t* err, const RowOut ro, int rows,
                                                            int n_q, int max_blocks, int fast_cap,
-                                                           int key_cap) {
-  extern __shared__ uint32_t sm[];
-  uint32_t* hist = sm;                           // [2048]
-  uint32_t* wsum = hist + 2048;                  // [2][32]
-  int* res = reinterpret_cast<int*>(wsum + 64);  // [8]
-  // bitmap path: cand_idx[kCandCap], cand_key[kCandCap], 2 bitmaps[fast_cap / 32]
+                                                           int key_cap, bool vec) {
+  extern __shared__ __align__(16) uint32_t sm[];
+  uint32_t* hist = sm;                                // [2048] digits 1 and 3
+  uint32_t* hist2 = hist + 2048;                      // [2048] digit 2
+  uint32_t* wsum = hist2 + 2048;                      // [2][32]
+  int* res = reinterpret_cast<int*>(wsum + 64);       // [8]
+  int32_t* blk = res + 8;                             // [512] the selection, ascending
+  int32_t* pt_s = blk + kTopK;                        // [kPtCap] the request's page table
   // long-row path: keys[key_cap]
   uint32_t* body = sm + kHdrWords;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
 
+  // Inputs of a row that do not come from the score kernel: its position and
+  // its request's page table (staged when it fits).
+  int p = 0;
+  bool pt_ok = false;
+  auto stage_row = [&](int row) {
+    p = q_pos[row];
+    const int r = row / n_q;
+    pt_ok = false;
+    if (ro.page_table && p >= 0) {
+      const int pages = min((p >> ro.page_shift) + 1, ro.max_pages);
+      if (pages <= kPtCap) {
+        pt_ok = true;
+        for (int i = tid; i < pages; i += kThreads) pt_s[i] = ro.page_table[(size_t)r * ro.max_pages + i];
+      }
+    }
+  };
+  for (int i = tid; i < 2 * kHistBins; i += kThreads) hist[i] = 0;
+  if (blockIdx.x < rows) stage_row(blockIdx.x);
+
   pdl_wait();  // the scores come from the previous kernel
   for (int row = blockIdx.x; row < rows; row += gridDim.x) {
-    const int p = q_pos[row];
+    if (row != (int)blockIdx.x) stage_row(row);
+    __syncthreads();  // staged page table and zeroed histograms
     int32_t* ob = sel_blk + (size_t)row * kTopK;
     int32_t* op = sel_pos + (size_t)row * kWidth;
     int32_t* orow = ro.page_table ? ro.sel_row + (size_t)row * kWidth : nullptr;
+    const int32_t* pt = pt_ok ? pt_s : nullptr;
     const int r = row / n_q, j = row - r * n_q;
     const bool p_ok = p >= 0 && n_full_of(p) <= max_blocks && (!orow || (p >> ro.page_shift) < ro.max_pages);
     const int n = p_ok ? n_full_of(p) : 0;
@@ -183,154 +203,169 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
       for (int i = tid; i < kTopK; i += kThreads) ob[i] = i < n ? i : -1;
       for (int i = tid; i < kWidth; i += kThreads) op[i] = (p_ok && i <= p) ? i : -1;
       if (orow)
-        for (int i = tid; i < kWidth; i += kThreads) orow[i] = (p_ok && i <= p) ? row_of(ro, r, i, err, j) : -1;
+        for (int i = tid; i < kWidth; i += kThreads) orow[i] = (p_ok && i <= p) ? row_of(ro, pt, r, i, err, j) : -1;
+      __syncthreads();  // shared memory is reused by the next row
       continue;
     }
     const int npart = (p + 1) & 3;
     const float* srow = scores + (size_t)row * max_blocks;
 
-    // pass 1: histogram of the top 11 key bits
-    const bool in_smem = n > fast_cap && n <= key_cap;  // long rows cache their keys
-    uint32_t* keys = body;
-    for (int i = tid; i < kHistBins; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    for_each_score(srow, n, [&](int i, uint32_t k) {
-      if (in_smem) keys[i] = k;
-      atomicAdd(&hist[k >> 21], 1u);
-    });
-    __syncthreads();
-    uint32_t need = kTopK;
-    find_bin<2048>(hist, need, wsum, res);
-    const uint32_t d1 = (uint32_t)res[0];
-    need -= (uint32_t)res[1];
-    const uint32_t nb = hist[d1];  // blocks in the threshold bin
+    if (n <= fast_cap) {
+      // ---- register path: thread t holds the keys of blocks [t kpt, t kpt + kpt) ----
+      // (in "virtual" indices v = i + off, where off makes 16-byte loads aligned)
+      const int off = vec ? (int)(((size_t)row * max_blocks) & 3) : 0;
+      const float* abase = srow - off;
+      const int span = n + off;
+      const int kpt = min(kKpt, (((span + kThreads - 1) / kThreads) + 3) & ~3);  // multiple of 4
+      const int v0 = tid * kpt;
+      const int lo = max(0, off - v0), hi = min(kpt, span - v0);  // valid entries [lo, hi)
+      const uint32_t valid_m = hi > lo ? ((hi >= 32 ? kFull : (1u << hi) - 1u) & ~((1u << lo) - 1u)) : 0u;
 
-    if (n <= fast_cap && nb <= (uint32_t)kCandCap) {
-      // ---- bitmap path: one pass over the scores, candidates = the threshold bin ----
-      const int nwords = (n + 31) >> 5;
-      uint32_t* cand_idx = body;
-      uint32_t* cand_key = cand_idx + kCandCap;
-      uint32_t* sel_bits = cand_key + kCandCap;       // surely selected, one bit per block
-      uint32_t* tie_bits = sel_bits + fast_cap / 32;  // equal to the threshold
-      if (tid == 0) res[4] = 0;
-      __syncthreads();
-      for (int w0 = warp; w0 < nwords; w0 += (kThreads / 32) * kBatch) {
-        float v[kBatch];
+      // pass 1: keys into registers, histogram of the top 11 bits
+      uint32_t key[kKpt];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int i = ((w0 + u * (kThreads / 32)) << 5) + lane;
-          v[u] = i < n ? srow[i] : 0.f;
+      for (int q = 0; q < kKpt / 4; ++q) {
+        if (4 * q >= kpt) break;  // block-uniform
+        const int v = v0 + 4 * q;
+        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (vec) {
+          if (v < span && v + 4 > off) f = *reinterpret_cast<const float4*>(abase + v);
+        } else {
+          if (v < span) f.x = abase[v];
+          if (v + 1 < span) f.y = abase[v + 1];
+          if (v + 2 < span) f.z = abase[v + 2];
+          if (v + 3 < span) f.w = abase[v + 3];
         }
+        key[4 * q + 0] = order_key(f.x);
+        key[4 * q + 1] = order_key(f.y);
+        key[4 * q + 2] = order_key(f.z);
+        key[4 * q + 3] = order_key(f.w);
+      }
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int w = w0 + u * (kThreads / 32);
-          if (w >= nwords) break;  // warp-uniform
-          const int i = (w << 5) + lane;
-          const uint32_t k = order_key(v[u]);
-          const uint32_t d = k >> 21;
-          const uint32_t gtm = __ballot_sync(kFull, i < n && d > d1);
-          const uint32_t cm = __ballot_sync(kFull, i < n && d == d1);
-          if (lane == 0) {
-            sel_bits[w] = gtm;
-            tie_bits[w] = 0u;
+      for (int e = 0; e < kKpt; ++e) {
+        if (e >= kpt) break;  // block-uniform
+        if ((valid_m >> e) & 1u) atomicAdd(&hist[key[e] >> 21], 1u);
+      }
+      __syncthreads();
+      uint32_t need = kTopK;
+      find_bin<2048>(hist, need, wsum, res);
+      const uint32_t d1 = (uint32_t)res[0];
+      need -= (uint32_t)res[1];
+
+      // pass 2: above the threshold bin / in it; histogram of digit 2 of the latter
+      uint32_t gt_m = 0, eq_m = 0;
+#pragma unroll
+      for (int e = 0; e < kKpt; ++e) {
+        if (e >= kpt) break;
+        const uint32_t d = key[e] >> 21;
+        gt_m |= (uint32_t)(d > d1) << e;
+        eq_m |= (uint32_t)(d == d1) << e;
+      }
+      gt_m &= valid_m;
+      eq_m &= valid_m;
+      if (eq_m) {
+#pragma unroll
+        for (int e = 0; e < kKpt; ++e) {
+          if (e >= kpt) break;
+          if ((eq_m >> e) & 1u) atomicAdd(&hist2[(key[e] >> 10) & 2047u], 1u);
+        }
+      }
+      for (int i = tid; i < 1024; i += kThreads) hist[i] = 0;
+      __syncthreads();
+      find_bin<2048>(hist2, need, wsum, res);
+      const uint32_t d2 = (uint32_t)res[0];
+      need -= (uint32_t)res[1];
+      const uint32_t prefix = (d1 << 11) | d2;
+      // when digit 2's bin is taken whole, no third digit is needed
+      const bool whole = hist2[d2] == need;
+      uint32_t T = prefix << 10;
+      if (!whole) {
+        // pass 3: digit 3 of the candidates sharing the prefix
+        if (eq_m) {
+#pragma unroll
+          for (int e = 0; e < kKpt; ++e) {
+            if (e >= kpt) break;
+            if (((eq_m >> e) & 1u) && (key[e] >> 10) == prefix) atomicAdd(&hist[key[e] & 1023u], 1u);
           }
-          if (cm) {
-            uint32_t base = 0;
-            if (lane == 0) base = atomicAdd(reinterpret_cast<uint32_t*>(&res[4]), (uint32_t)__popc(cm));
-            base = __shfl_sync(kFull, base, 0);
-            const uint32_t slot = base + (uint32_t)__popc(cm & lt_mask);
-            if ((cm & (1u << lane)) && slot < (uint32_t)kCandCap) {
-              cand_idx[slot] = (uint32_t)i;
-              cand_key[slot] = k;
-            }
+        }
+        __syncthreads();
+        find_bin<1024>(hist, need, wsum, res);
+        T |= (uint32_t)res[0];
+        need -= (uint32_t)res[1];  // blocks equal to T still to take, >= 1
+      } else {
+        need = 0;
+      }
+      // selected (above T, or the whole digit-2 bin) and tied (equal to T)
+      uint32_t sel_m = gt_m, tie_m = 0;
+      if (eq_m) {
+#pragma unroll
+        for (int e = 0; e < kKpt; ++e) {
+          if (e >= kpt) break;
+          if ((eq_m >> e) & 1u) {
+            const uint32_t k = key[e];
+            if (whole ? (k >> 10) >= prefix : k > T) sel_m |= 1u << e;
+            else if (!whole && k == T) tie_m |= 1u << e;
           }
         }
       }
+      // thread order is index order: one scan lists the selection ascending,
+      // the lowest-index ties first
+      uint32_t total;
+      const uint32_t excl = block_excl_scan(((uint32_t)__popc(tie_m) << 16) | (uint32_t)__popc(sel_m), wsum, &total);
+      const uint32_t e_before = excl >> 16, s_before = excl & 0xffffu;
+      uint32_t take = need > e_before ? min(need - e_before, (uint32_t)__popc(tie_m)) : 0u;
+      uint32_t slot = s_before + min(e_before, need);
+      if (sel_m | tie_m) {
+#pragma unroll
+        for (int e = 0; e < kKpt; ++e) {
+          if (e >= kpt) break;
+          bool pick = (sel_m >> e) & 1u;
+          if (!pick && ((tie_m >> e) & 1u) && take > 0) {
+            pick = true;
+            --take;
+          }
+          if (pick) {
+            if (slot < (uint32_t)kTopK) blk[slot] = v0 + e - off;  // exactly kTopK; the bound is a guard
+            ++slot;
+          }
+        }
+      }
+    } else {
+      // ---- long rows: radix passes over the whole row ----
+      const bool in_smem = n <= key_cap;  // keys cached in shared memory
+      uint32_t* keys = body;
+      for_each_score(srow, n, [&](int i, bool ok, uint32_t k) {
+        if (in_smem && ok) keys[i] = k;
+        hist_add(hist, ok, k >> 21, lane);
+      });
+      __syncthreads();
+      uint32_t need = kTopK;
+      find_bin<2048>(hist, need, wsum, res);
+      const uint32_t d1 = (uint32_t)res[0];
+      need -= (uint32_t)res[1];
       for (int i = tid; i < 2048; i += kThreads) hist[i] = 0;
       __syncthreads();
-      const int nc = min(res[4], kCandCap);
-      // pass 2 over the candidates: key bits 20..10
-      for (int c = tid; c < nc; c += kThreads) atomicAdd(&hist[(cand_key[c] >> 10) & 2047u], 1u);
+      auto key_at = [&](int i) { return in_smem ? keys[i] : order_key(srow[i]); };
+      for (int i = tid; i < n; i += kThreads) {
+        const uint32_t k = key_at(i);
+        if ((k >> 21) == d1) atomicAdd(&hist[(k >> 10) & 2047u], 1u);
+      }
       __syncthreads();
       find_bin<2048>(hist, need, wsum, res);
       const uint32_t prefix = (d1 << 11) | (uint32_t)res[0];
       need -= (uint32_t)res[1];
       for (int i = tid; i < 1024; i += kThreads) hist[i] = 0;
       __syncthreads();
-      // pass 3: key bits 9..0
-      for (int c = tid; c < nc; c += kThreads) {
-        const uint32_t k = cand_key[c];
+      for (int i = tid; i < n; i += kThreads) {
+        const uint32_t k = key_at(i);
         if ((k >> 10) == prefix) atomicAdd(&hist[k & 1023u], 1u);
       }
       __syncthreads();
       find_bin<1024>(hist, need, wsum, res);
       const uint32_t T = (prefix << 10) | (uint32_t)res[0];
-      need -= (uint32_t)res[1];  // blocks equal to T still to take, >= 1
-      for (int c = tid; c < nc; c += kThreads) {
-        const uint32_t i = cand_idx[c];
-        const uint32_t k = cand_key[c];
-        if (k > T) atomicOr(&sel_bits[i >> 5], 1u << (i & 31));
-        else if (k == T) atomicOr(&tie_bits[i >> 5], 1u << (i & 31));
-      }
-      __syncthreads();
-      // one word of 32 blocks per thread, in index order
-      uint32_t s = 0, e = 0;
-      if (tid < nwords) {
-        s = sel_bits[tid];
-        e = tie_bits[tid];
-      }
-      uint32_t total;
-      const uint32_t excl = block_excl_scan(((uint32_t)__popc(e) << 16) | (uint32_t)__popc(s), wsum, &total);
-      const uint32_t e_before = excl >> 16, s_before = excl & 0xffffu;
-      const uint32_t taken_before = min(e_before, need);
-      uint32_t take = need > e_before ? min(need - e_before, (uint32_t)__popc(e)) : 0u;
-      uint32_t rest = e;
-      for (uint32_t t = 0; t < take; ++t) rest &= rest - 1u;  // drop the lowest `take` ties
-      uint32_t word = s | (e ^ rest);
-      uint32_t slot = s_before + taken_before;
-      while (word) {
-        const int b = __ffs(word) - 1;
-        write_block(ob, op, orow, ro, err, r, j, slot++, (tid << 5) + b);
-        word &= word - 1u;
-      }
-    } else {
-      // ---- long rows (or a crowded threshold bin): radix passes over the whole row ----
-      __syncthreads();  // every thread has read hist[d1]
-      for (int i = tid; i < 2048; i += kThreads) hist[i] = 0;
-      __syncthreads();
-      auto key_at = [&](int i) { return in_smem ? keys[i] : order_key(srow[i]); };
-      if (in_smem) {
-        for (int i = tid; i < n; i += kThreads) {
-          const uint32_t k = keys[i];
-          if ((k >> 21) == d1) atomicAdd(&hist[(k >> 10) & 2047u], 1u);
-        }
-      } else {
-        for_each_score(srow, n, [&](int, uint32_t k) {
-          if ((k >> 21) == d1) atomicAdd(&hist[(k >> 10) & 2047u], 1u);
-        });
-      }
-      __syncthreads();
-      find_bin<2048>(hist, need, wsum, res);
-      const uint32_t prefix = (d1 << 11) | (uint32_t)res[0];
-      need -= (uint32_t)res[1];
-      for (int i = tid; i < 1024; i += kThreads) hist[i] = 0;
-      __syncthreads();
-      if (in_smem) {
-        for (int i = tid; i < n; i += kThreads) {
-          const uint32_t k = keys[i];
-          if ((k >> 10) == prefix) atomicAdd(&hist[k & 1023u], 1u);
-        }
-      } else {
-        for_each_score(srow, n, [&](int, uint32_t k) {
-          if ((k >> 10) == prefix) atomicAdd(&hist[k & 1023u], 1u);
-        });
-      }
-      __syncthreads();
-      find_bin<1024>(hist, need, wsum, res);
-      const uint32_t T = (prefix << 10) | (uint32_t)res[0];
       need -= (uint32_t)res[1];
 
-      // ordered compaction: keys > T, then the first `need` keys == T
+      // ordered listing: keys > T, then the first `need` keys == T
       uint32_t n_sel = 0, n_tie = 0;
       int buf = 0;
       for (int base = 0; base < n; base += kThreads) {
@@ -346,25 +381,33 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
         const uint32_t c = wc[lane];
         const uint32_t incl = warp_incl_scan(c, lane);
         const uint32_t excl_w = __shfl_sync(kFull, incl - c, warp);
-        const uint32_t total = __shfl_sync(kFull, incl, 31);
+        const uint32_t tot = __shfl_sync(kFull, incl, 31);
         const uint32_t E_w = excl_w >> 16, G_w = excl_w & 0xffffu;
-        const uint32_t E_t = total >> 16, G_t = total & 0xffffu;
+        const uint32_t E_t = tot >> 16, G_t = tot & 0xffffu;
         const uint32_t rem_tile = need > n_tie ? need - n_tie : 0u;
         const uint32_t taken_before = min(rem_tile, E_w);
         const uint32_t rem_w = rem_tile > E_w ? rem_tile - E_w : 0u;
         const uint32_t my_eq = (uint32_t)__popc(eqm & lt_mask);
-        if (gt || (eq && my_eq < rem_w))
-          write_block(ob, op, orow, ro, err, r, j,
-                      n_sel + G_w + taken_before + (uint32_t)__popc(gtm & lt_mask) + min(my_eq, rem_w), i);
+        if (gt || (eq && my_eq < rem_w)) {
+          const uint32_t slot = n_sel + G_w + taken_before + (uint32_t)__popc(gtm & lt_mask) + min(my_eq, rem_w);
+          if (slot < (uint32_t)kTopK) blk[slot] = i;
+        }
         n_sel += G_t + min(rem_tile, E_t);
         n_tie += E_t;
         buf ^= 1;
       }
     }
-    if (tid < kBlock - 1) {
-      op[kBlock * kTopK + tid] = tid < npart ? kBlock * n + tid : -1;
-      if (orow) orow[kBlock * kTopK + tid] = tid < npart ? row_of(ro, r, kBlock * n + tid, err, j) : -1;
+    __syncthreads();  // the selection list is complete
+    // outputs, coalesced: block ids, their positions (then the unfilled block's), cache rows
+    for (int i = tid; i < kTopK; i += kThreads) ob[i] = blk[i];
+    for (int i = tid; i < kWidth; i += kThreads) {
+      int pos;
+      if (i < kBlock * kTopK) pos = kBlock * blk[i >> 2] + (i & 3);
+      else pos = (i - kBlock * kTopK < npart) ? kBlock * n + (i - kBlock * kTopK) : -1;
+      op[i] = pos;
+      if (orow) orow[i] = pos < 0 ? -1 : row_of(ro, pt, r, pos, err, j);
     }
+    for (int i = tid; i < 2 * kHistBins; i += kThreads) hist[i] = 0;
     __syncthreads();  // shared memory is reused by the next row
   }
   pdl_trigger();
@@ -382,9 +425,7 @@ cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q
   const int mb32 = (mb + 31) / 32 * 32;
   const int fast_cap = mb <= kTopK ? 0 : (mb32 < kFastCap ? mb32 : kFastCap);
   const int key_cap = mb > kFastCap ? (mb < kKeyCap ? mb : kKeyCap) : 0;
-  const size_t fast_words = fast_cap ? (size_t)2 * kCandCap + 2 * (fast_cap / 32) : 0;
-  const size_t long_words = (size_t)key_cap;
-  const size_t body = fast_words > long_words ? fast_words : long_words;
+  const size_t body = (size_t)key_cap;  // the register path needs no body
   const size_t smem = (kHdrWords + body) * sizeof(uint32_t);
   static size_t set_bytes[64] = {0};
   int dev = 0;
@@ -406,7 +447,8 @@ cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q
   ro.page_shift = shift;
   ro.n_kv = d.n_kv_heads;
   return launch_k(topk_kernel, dim3(grid), dim3(kThreads), smem, s, pdl, scores, q_pos, sel_blk,
-                  sel_pos, err, ro, rows, d.n_q, d.max_blocks, fast_cap, key_cap);
+                  sel_pos, err, ro, rows, d.n_q, d.max_blocks, fast_cap, key_cap,
+                  (reinterpret_cast<uintptr_t>(scores) & 15u) == 0);
 }
 
 }  // namespace qsa
