@@ -33,7 +33,7 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kKpt = 24;         // keys per thread on the register path
+constexpr int kKpt = 24;         // most keys per thread on the register path
 constexpr int kFastCap = kKpt * kThreads - 4;  // longest row on it (3 blocks of alignment slack)
 constexpr int kKeyCap = 49152;   // keys cached in shared memory on the long-row path
 constexpr int kPtCap = 4096;     // page-table entries staged in shared memory
@@ -148,6 +148,122 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, bool valid, uint32_t bi
   if (valid) atomicAdd(&hist[bin], 1u);
 }
 
+// The register path for one row: thread t holds the keys of blocks
+// [t KPT, t KPT + KPT) in "virtual" indices v = i + off, where off makes the
+// 16-byte loads aligned. Lists the row's kTopK selected blocks, ascending,
+// in blk. Starts after a barrier (zeroed histograms); ends with one.
+template <int KPT>
+__device__ __forceinline__ void select_regs(const float* srow, int n, int off, bool vec, uint32_t* hist,
+                                            uint32_t* hist2, uint32_t* wsum, int* res, int32_t* blk) {
+  const int tid = threadIdx.x;
+  const int span = n + off;
+  const int v0 = tid * KPT;
+  const int lo = max(0, off - v0), hi = min(KPT, span - v0);  // valid entries [lo, hi)
+  constexpr uint32_t kAll = (1u << KPT) - 1u;
+  const uint32_t valid_m = hi > lo ? (kAll >> (KPT - hi)) & ~((1u << lo) - 1u) : 0u;
+  const float* abase = srow - off;
+
+  // pass 1: keys into registers, histogram of the top 11 bits
+  uint32_t key[KPT];
+#pragma unroll
+  for (int q = 0; q < KPT / 4; ++q) {
+    const int v = v0 + 4 * q;
+    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (vec) {
+      if (v < span && v + 4 > off) f = *reinterpret_cast<const float4*>(abase + v);
+    } else {
+      if (v < span) f.x = abase[v];
+      if (v + 1 < span) f.y = abase[v + 1];
+      if (v + 2 < span) f.z = abase[v + 2];
+      if (v + 3 < span) f.w = abase[v + 3];
+    }
+    key[4 * q + 0] = order_key(f.x);
+    key[4 * q + 1] = order_key(f.y);
+    key[4 * q + 2] = order_key(f.z);
+    key[4 * q + 3] = order_key(f.w);
+  }
+  if (valid_m == kAll) {
+#pragma unroll
+    for (int e = 0; e < KPT; ++e) atomicAdd(&hist[key[e] >> 21], 1u);
+  } else if (valid_m) {
+#pragma unroll
+    for (int e = 0; e < KPT; ++e)
+      if ((valid_m >> e) & 1u) atomicAdd(&hist[key[e] >> 21], 1u);
+  }
+  __syncthreads();
+  uint32_t need = kTopK;
+  find_bin<2048>(hist, need, wsum, res);
+  const uint32_t d1 = (uint32_t)res[0];
+  need -= (uint32_t)res[1];
+
+  // pass 2: keys above the threshold bin / in it; digit 2 of the latter
+  const uint32_t lo_key = d1 << 21;                                 // first key of bin d1
+  const uint32_t hi_key = d1 == 2047u ? 0xffffffffu : ((d1 + 1u) << 21) - 1u;  // its last key
+  uint32_t gt_m = 0, eq_m = 0;
+#pragma unroll
+  for (int e = 0; e < KPT; ++e) {
+    gt_m |= (uint32_t)(key[e] > hi_key) << e;
+    eq_m |= (uint32_t)(key[e] >= lo_key) << e;
+  }
+  gt_m &= valid_m;
+  eq_m &= valid_m & ~gt_m;
+  if (eq_m) {
+#pragma unroll
+    for (int e = 0; e < KPT; ++e)
+      if ((eq_m >> e) & 1u) atomicAdd(&hist2[(key[e] >> 10) & 2047u], 1u);
+  }
+  for (int i = tid; i < 1024; i += kThreads) hist[i] = 0;
+  __syncthreads();
+  find_bin<2048>(hist2, need, wsum, res);
+  const uint32_t d2 = (uint32_t)res[0];
+  need -= (uint32_t)res[1];
+  const uint32_t prefix = (d1 << 11) | d2;
+  // when digit 2's bin is taken whole, no third digit is needed
+  const bool whole = hist2[d2] == need;
+  uint32_t T = prefix << 10;
+  if (!whole) {
+    // pass 3: digit 3 of the candidates sharing the prefix
+    if (eq_m) {
+#pragma unroll
+      for (int e = 0; e < KPT; ++e)
+        if (((eq_m >> e) & 1u) && (key[e] >> 10) == prefix) atomicAdd(&hist[key[e] & 1023u], 1u);
+    }
+    __syncthreads();
+    find_bin<1024>(hist, need, wsum, res);
+    T |= (uint32_t)res[0];
+    need -= (uint32_t)res[1];  // blocks equal to T still to take, >= 1
+  } else {
+    need = 0;
+  }
+  // selected (above T, or the whole digit-2 bin) and tied (equal to T)
+  uint32_t sel_m = gt_m, tie_m = 0;
+  if (eq_m) {
+    const uint32_t cut = whole ? T : T + 1u;  // selected: key >= cut (T < 2^32 - 1 here)
+#pragma unroll
+    for (int e = 0; e < KPT; ++e) {
+      const bool in = (eq_m >> e) & 1u;
+      sel_m |= (uint32_t)(in && key[e] >= cut) << e;
+      tie_m |= (uint32_t)(in && !whole && key[e] == T) << e;
+    }
+  }
+  // thread order is index order: one scan lists the selection ascending,
+  // the lowest-index ties first
+  uint32_t total;
+  const uint32_t excl = block_excl_scan(((uint32_t)__popc(tie_m) << 16) | (uint32_t)__popc(sel_m), wsum, &total);
+  const uint32_t e_before = excl >> 16, s_before = excl & 0xffffu;
+  uint32_t take = need > e_before ? min(need - e_before, (uint32_t)__popc(tie_m)) : 0u;
+  uint32_t rest = tie_m;
+  for (; take > 0; --take) rest &= rest - 1u;  // drop the lowest `take` ties: they are taken
+  uint32_t pick = sel_m | (tie_m ^ rest);
+  uint32_t slot = s_before + min(e_before, need);
+  while (pick) {
+    const int e = __ffs(pick) - 1;
+    if (slot < (uint32_t)kTopK) blk[slot] = v0 + e - off;  // exactly kTopK; the bound is a guard
+    ++slot;
+    pick &= pick - 1u;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restrict__ scores,
                                                            const int32_t* __restrict__ q_pos,
                                                            int32_t* __restrict__ sel_blk,
@@ -211,125 +327,15 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
     const float* srow = scores + (size_t)row * max_blocks;
 
     if (n <= fast_cap) {
-      // ---- register path: thread t holds the keys of blocks [t kpt, t kpt + kpt) ----
-      // (in "virtual" indices v = i + off, where off makes 16-byte loads aligned)
+      // ---- register path ----
       const int off = vec ? (int)(((size_t)row * max_blocks) & 3) : 0;
-      const float* abase = srow - off;
       const int span = n + off;
-      const int kpt = min(kKpt, (((span + kThreads - 1) / kThreads) + 3) & ~3);  // multiple of 4
-      const int v0 = tid * kpt;
-      const int lo = max(0, off - v0), hi = min(kpt, span - v0);  // valid entries [lo, hi)
-      const uint32_t valid_m = hi > lo ? ((hi >= 32 ? kFull : (1u << hi) - 1u) & ~((1u << lo) - 1u)) : 0u;
-
-      // pass 1: keys into registers, histogram of the top 11 bits
-      uint32_t key[kKpt];
-#pragma unroll
-      for (int q = 0; q < kKpt / 4; ++q) {
-        if (4 * q >= kpt) break;  // block-uniform
-        const int v = v0 + 4 * q;
-        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (vec) {
-          if (v < span && v + 4 > off) f = *reinterpret_cast<const float4*>(abase + v);
-        } else {
-          if (v < span) f.x = abase[v];
-          if (v + 1 < span) f.y = abase[v + 1];
-          if (v + 2 < span) f.z = abase[v + 2];
-          if (v + 3 < span) f.w = abase[v + 3];
-        }
-        key[4 * q + 0] = order_key(f.x);
-        key[4 * q + 1] = order_key(f.y);
-        key[4 * q + 2] = order_key(f.z);
-        key[4 * q + 3] = order_key(f.w);
-      }
-#pragma unroll
-      for (int e = 0; e < kKpt; ++e) {
-        if (e >= kpt) break;  // block-uniform
-        if ((valid_m >> e) & 1u) atomicAdd(&hist[key[e] >> 21], 1u);
-      }
-      __syncthreads();
-      uint32_t need = kTopK;
-      find_bin<2048>(hist, need, wsum, res);
-      const uint32_t d1 = (uint32_t)res[0];
-      need -= (uint32_t)res[1];
-
-      // pass 2: above the threshold bin / in it; histogram of digit 2 of the latter
-      uint32_t gt_m = 0, eq_m = 0;
-#pragma unroll
-      for (int e = 0; e < kKpt; ++e) {
-        if (e >= kpt) break;
-        const uint32_t d = key[e] >> 21;
-        gt_m |= (uint32_t)(d > d1) << e;
-        eq_m |= (uint32_t)(d == d1) << e;
-      }
-      gt_m &= valid_m;
-      eq_m &= valid_m;
-      if (eq_m) {
-#pragma unroll
-        for (int e = 0; e < kKpt; ++e) {
-          if (e >= kpt) break;
-          if ((eq_m >> e) & 1u) atomicAdd(&hist2[(key[e] >> 10) & 2047u], 1u);
-        }
-      }
-      for (int i = tid; i < 1024; i += kThreads) hist[i] = 0;
-      __syncthreads();
-      find_bin<2048>(hist2, need, wsum, res);
-      const uint32_t d2 = (uint32_t)res[0];
-      need -= (uint32_t)res[1];
-      const uint32_t prefix = (d1 << 11) | d2;
-      // when digit 2's bin is taken whole, no third digit is needed
-      const bool whole = hist2[d2] == need;
-      uint32_t T = prefix << 10;
-      if (!whole) {
-        // pass 3: digit 3 of the candidates sharing the prefix
-        if (eq_m) {
-#pragma unroll
-          for (int e = 0; e < kKpt; ++e) {
-            if (e >= kpt) break;
-            if (((eq_m >> e) & 1u) && (key[e] >> 10) == prefix) atomicAdd(&hist[key[e] & 1023u], 1u);
-          }
-        }
-        __syncthreads();
-        find_bin<1024>(hist, need, wsum, res);
-        T |= (uint32_t)res[0];
-        need -= (uint32_t)res[1];  // blocks equal to T still to take, >= 1
-      } else {
-        need = 0;
-      }
-      // selected (above T, or the whole digit-2 bin) and tied (equal to T)
-      uint32_t sel_m = gt_m, tie_m = 0;
-      if (eq_m) {
-#pragma unroll
-        for (int e = 0; e < kKpt; ++e) {
-          if (e >= kpt) break;
-          if ((eq_m >> e) & 1u) {
-            const uint32_t k = key[e];
-            if (whole ? (k >> 10) >= prefix : k > T) sel_m |= 1u << e;
-            else if (!whole && k == T) tie_m |= 1u << e;
-          }
-        }
-      }
-      // thread order is index order: one scan lists the selection ascending,
-      // the lowest-index ties first
-      uint32_t total;
-      const uint32_t excl = block_excl_scan(((uint32_t)__popc(tie_m) << 16) | (uint32_t)__popc(sel_m), wsum, &total);
-      const uint32_t e_before = excl >> 16, s_before = excl & 0xffffu;
-      uint32_t take = need > e_before ? min(need - e_before, (uint32_t)__popc(tie_m)) : 0u;
-      uint32_t slot = s_before + min(e_before, need);
-      if (sel_m | tie_m) {
-#pragma unroll
-        for (int e = 0; e < kKpt; ++e) {
-          if (e >= kpt) break;
-          bool pick = (sel_m >> e) & 1u;
-          if (!pick && ((tie_m >> e) & 1u) && take > 0) {
-            pick = true;
-            --take;
-          }
-          if (pick) {
-            if (slot < (uint32_t)kTopK) blk[slot] = v0 + e - off;  // exactly kTopK; the bound is a guard
-            ++slot;
-          }
-        }
-      }
+      if (span <= 4 * kThreads) select_regs<4>(srow, n, off, vec, hist, hist2, wsum, res, blk);
+      else if (span <= 8 * kThreads) select_regs<8>(srow, n, off, vec, hist, hist2, wsum, res, blk);
+      else if (span <= 12 * kThreads) select_regs<12>(srow, n, off, vec, hist, hist2, wsum, res, blk);
+      else if (span <= 16 * kThreads) select_regs<16>(srow, n, off, vec, hist, hist2, wsum, res, blk);
+      else if (span <= 20 * kThreads) select_regs<20>(srow, n, off, vec, hist, hist2, wsum, res, blk);
+      else select_regs<24>(srow, n, off, vec, hist, hist2, wsum, res, blk);
     } else {
       // ---- long rows: radix passes over the whole row ----
       const bool in_smem = n <= key_cap;  // keys cached in shared memory
