@@ -484,6 +484,7 @@ __global__ void __launch_bounds__(256) resolve_kernel(const int32_t* __restrict_
                                                       int32_t* __restrict__ sel_row, int32_t* err, int n_q,
                                                       int n_kv, int page_shift, int max_pages, int num_pages,
                                                       int width) {
+  pdl_trigger();  // the attention kernel waits for this whole grid anyway
   const int row = blockIdx.x, r = row / n_q, j = row - r * n_q;
   const int p = q_pos[row];
   const bool p_ok = p >= 0 && (p >> page_shift) < max_pages;
@@ -505,7 +506,6 @@ __global__ void __launch_bounds__(256) resolve_kernel(const int32_t* __restrict_
     }
     sel_row[(size_t)row * width + i] = ri;
   }
-  pdl_trigger();
 }
 
 int page_shift_of(int page_size) {

@@ -136,6 +136,9 @@ __global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(cons
   extern __shared__ int s_off[];  // [B + 1] first unit (16 blocks) of each request
 
   pdl_wait();  // no-op unless launched as a dependent
+  // Let the selector launch now: its CTAs take each SM as this kernel's CTA
+  // there exits, and its own wait still covers all of this grid's scores.
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   if (threadIdx.x < 32) {
     int carry = 0;
@@ -249,7 +252,6 @@ __global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(cons
     }
     u = seg_end;  // the unrolled loop may step past the end of this request's units
   }
-  pdl_trigger();
 }
 
 template <int H>

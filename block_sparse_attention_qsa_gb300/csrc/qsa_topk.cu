@@ -303,6 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
   if (blockIdx.x < rows) stage_row(blockIdx.x);
 
   pdl_wait();  // the scores come from the previous kernel
+  // Let the attention kernel launch now: its CTAs wait on the SMs this grid
+  // leaves free, and their own wait still covers every selection written here.
+  pdl_trigger();
   for (int row = blockIdx.x; row < rows; row += gridDim.x) {
     if (row != (int)blockIdx.x) stage_row(row);
     __syncthreads();  // staged page table and zeroed histograms
@@ -416,7 +419,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
     for (int i = tid; i < 2 * kHistBins; i += kThreads) hist[i] = 0;
     __syncthreads();  // shared memory is reused by the next row
   }
-  pdl_trigger();
 }
 
 }  // namespace
