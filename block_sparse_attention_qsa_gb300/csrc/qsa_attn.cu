@@ -7,33 +7,37 @@
 // found in the cache. The geometry here is theirs as this library reads it:
 // 16 query heads over 2 KV heads of dim 128, a paged cache of 64-token pages.
 //
-// Design. One CTA of 4 warps per (request, query, KV head, split of the
-// selection buffer). The CTA resolves its positions to cache rows through the
-// page table once; from then on every warp works alone on 8 positions of
-// each 32-position tile. The selected K/V rows are random 256-byte (BF16) or
-// 128-byte (FP8) rows, so the kernel is a gather: measured on GB300, 128-bit
-// loads straight into registers, with each warp reading whole rows, sustain a
-// much higher share of HBM bandwidth for such gathers than staging through
-// shared memory. So K and V never touch shared memory:
+// Design (stream-K). The (request, query, KV head) units times their tiles
+// of selected positions form one stream of tiles, cut into equal contiguous
+// shares, one per resident 4-warp CTA, so every CTA does the same work and
+// the kernel has no wave tail. Within a tile every warp works alone on 8
+// positions (BF16) or 16 (FP8, so that a step moves as many bytes). The
+// selected K/V rows are random 256-byte (BF16) or 128-byte (FP8) rows, so the
+// kernel is a gather: measured on GB300, 128-bit loads straight into
+// registers, with each warp reading whole rows, sustain a much higher share
+// of HBM bandwidth for such gathers than staging through shared memory. So K
+// and V never touch shared memory:
 //
 //  * S^T = K Q^T on the tensor cores (mma.sync m16n8k16, FP32 accumulate):
-//    the warp's 8 positions are the M rows, the KV group's 8 query heads the
-//    N columns. A lane's 16-byte loads of K rows are its A fragments directly,
-//    because the head dim is visited in a lane-dependent order that Q's B
-//    fragments follow too (a dot product does not depend on the order of its
-//    terms).
+//    the warp's positions are the M rows (BF16: rows 0..7, FP8: 0..15), the
+//    KV group's 8 query heads the N columns. A lane's 16-byte loads of K rows
+//    are its A fragments directly, because the head dim is visited in a
+//    lane-dependent order that Q's B fragments follow too (a dot product does
+//    not depend on the order of its terms).
 //  * softmax is online, in FP32, in the exp2 domain, per head;
 //  * O^T = V^T P^T: V rows loaded the same way are turned into A fragments
 //    with movmatrix (an in-register 8x8 transpose), P^T is the softmax tile
 //    transposed the same way, and the output's dim order (permuted by the V
 //    loads) is undone when it is written.
 //
-// FP8 rows are widened to FP16 in registers (exact for E4M3); K's scale
-// folds into the softmax scale and V's into the output. The warps' softmax
-// states merge through shared memory; splits write (max, sum, acc) partials
-// to the workspace and the last CTA of a (request, query, KV head) to arrive,
-// counted by an atomic ticket, merges them and resets the ticket, so there is
-// no spin-wait anywhere.
+// Each lane looks two tiles ahead in the selection, so the K/V loads of the
+// next tile are in flight across unit boundaries. FP8 codes stay packed in
+// registers and are widened to FP16 (exact for E4M3) right before their mma;
+// K's scale folds into the softmax scale and V's into the output. The warps'
+// softmax states merge through shared memory; a unit split between CTAs
+// publishes (max, sum, acc) pieces to the workspace and the last piece to
+// arrive, counted by an atomic ticket, merges them and resets the ticket, so
+// there is no spin-wait anywhere.
 #include <cuda_fp8.h>
 
 #include "qsa_internal.cuh"
@@ -41,8 +45,7 @@
 namespace qsa {
 namespace {
 
-constexpr int kWarpPos = 8;     // positions per warp step
-constexpr int kTile = 4 * kWarpPos;  // positions per CTA step: 4 warps
+constexpr int kTile = 32;       // BF16 positions per CTA step: 4 warps of 8 (FP8: 4 of 16)
 constexpr int kThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -114,33 +117,29 @@ __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) {
 // Register layout of one lane's share of a 128-dim row, for lane = 4g + c.
 //   BF16 rows (256 B): 4 loads of 16 B at chunks c, c+4, c+8, c+12 -> 16
 //   pairs; pair (i, e) holds dims 8(c + 4i) + 2e + {0,1}.
-//   FP8 rows (128 B): 2 loads of 16 B at chunks c, c+4 -> 16 pairs after
-//   widening; pair (i, e) holds dims 16(c + 4i) + 2e + {0,1}.
+//   FP8 rows (128 B): 2 loads of 16 B at chunks c, c+4, kept as 8 raw words
+//   of 4 E4M3 codes; pair (i, e) holds dims 16(c + 4i) + 2e + {0,1} and is the
+//   low (e even) or high half of raw word 4i + e/2, widened to FP16 (exact)
+//   where it is used.
 // Pair p = 4i + e (BF16) or 8i + e (FP8) is the lane's p-th pair.
-//   K: k-step ks (16 of the 128 dims) uses pairs 2ks and 2ks + 1 of a row.
-//   V: the 8x8 block k (logical dims 8k..8k+7) holds pair k of each row.
+//   K: k-step ks (16 of the 128 dims) uses pairs 2ks and 2ks + 1 of a row
+//      (FP8: the two halves of raw word ks).
+//   V: the 8x8 block k (logical dims 8k..8k+7) holds pair k of each row
+//      (FP8: blocks 2m and 2m + 1 are the two halves of raw word m).
 template <bool FP8>
 struct RowRegs {
   static constexpr int kLoads = FP8 ? 2 : 4;
   static constexpr int kRowBytes = FP8 ? 128 : 256;
-  uint32_t pr[16];  // 16 pairs of 16-bit values
+  uint32_t pr[FP8 ? 8 : 16];  // BF16: 16 pairs; FP8: 8 raw words (16 pairs of codes)
 
   __device__ __forceinline__ void load(const uint8_t* row, int c, bool ok) {
-    uint4 raw[kLoads];
-#pragma unroll
-    for (int i = 0; i < kLoads; ++i) raw[i] = ok ? ldg16(row + (c + 4 * i) * 16) : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int i = 0; i < kLoads; ++i) {
-      const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if constexpr (FP8) {
-          pr[8 * i + 2 * e] = e4m3x2_to_h2(w[e]);
-          pr[8 * i + 2 * e + 1] = e4m3x2_to_h2(w[e] >> 16);
-        } else {
-          pr[4 * i + e] = w[e];
-        }
-      }
+      const uint4 v = ok ? ldg16(row + (c + 4 * i) * 16) : make_uint4(0, 0, 0, 0);
+      pr[4 * i + 0] = v.x;
+      pr[4 * i + 1] = v.y;
+      pr[4 * i + 2] = v.z;
+      pr[4 * i + 3] = v.w;
     }
   }
 };
@@ -189,9 +188,13 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const AttnArgs a) {
   __shared__ float s_ml[96];
   __shared__ int s_last;
 
+  // positions per warp step: 8 for BF16 (rows g of the mma), 16 for FP8
+  // (rows g and g + 8), so that an FP8 step moves as many bytes as a BF16 one
+  constexpr int POS = FP8 ? 16 : 8;
+  constexpr int TILE = 4 * POS;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gq = lane >> 2, c4 = lane & 3;
-  const int ent = warp * kWarpPos + gq;  // this lane's position within a tile
+  const int ent = warp * POS + gq;  // this lane's position within a tile (FP8: and ent + 8)
   const int n_q_heads = a.n_kv * kGroup;
   const int P = a.page_size;
   using RR = RowRegs<FP8>;
@@ -221,8 +224,8 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const AttnArgs a) {
   // Row look-ahead: the selection entries of tile w + 2 are loaded while tile w
   // is processed, and turn into cache rows for the K/V loads of tile w + 1.
   Cursor L{t, u % a.n_kv, u / a.n_kv};
-  auto load_entry = [&](bool in_range) {
-    const int i = L.t * kTile + ent;
+  auto load_entry = [&](bool in_range, int off) {
+    const int i = L.t * TILE + ent + off;
     return (in_range && i < a.width) ? ld_issue(a.sel_row + (size_t)L.row * a.width + i) : -1;
   };
   auto advance = [&]() {
@@ -234,16 +237,21 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const AttnArgs a) {
       }
     }
   };
-  const int e0 = load_entry(true), g0 = L.g;
+  const int e0 = load_entry(true, 0), e0h = FP8 ? load_entry(true, 8) : -1, g0 = L.g;
   advance();
-  int e1 = load_entry(w0 + 1 < w1), g1 = L.g;
+  int e1 = load_entry(w0 + 1 < w1, 0), e1h = FP8 ? load_entry(w0 + 1 < w1, 8) : -1, g1 = L.g;
   advance();
   long long wl = w0 + 2;  // tile of the cursor
 
-  RR kr, vr;
+  RR kr, vr, krh, vrh;  // krh, vrh: rows g + 8 (FP8 only)
   int ri = e0 >= 0 ? e0 + g0 * P : -1;
+  int rih = e0h >= 0 ? e0h + g0 * P : -1;
   kr.load(kbase + (size_t)max(ri, 0) * RR::kRowBytes, c4, ri >= 0);
   vr.load(vbase + (size_t)max(ri, 0) * RR::kRowBytes, c4, ri >= 0);
+  if constexpr (FP8) {
+    krh.load(kbase + (size_t)max(rih, 0) * RR::kRowBytes, c4, rih >= 0);
+    vrh.load(vbase + (size_t)max(rih, 0) * RR::kRowBytes, c4, rih >= 0);
+  }
 
   long long w = w0;
   for (int buf = 0;; buf ^= 1) {
@@ -290,23 +298,39 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const AttnArgs a) {
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
     for (int i = 0; i < seg; ++i, ++w) {
-      // S^T (8 positions x 8 heads)
+      // S^T (POS positions x 8 heads)
       float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) mma16816<FP8>(s, kr.pr[2 * ks], 0u, kr.pr[2 * ks + 1], 0u, qb[2 * ks], qb[2 * ks + 1]);
-      const bool ok = ri >= 0;
+      for (int ks = 0; ks < 8; ++ks) {
+        if constexpr (FP8) {
+          const uint32_t wl0 = kr.pr[ks], wh0 = krh.pr[ks];
+          mma16816<true>(s, e4m3x2_to_h2(wl0), e4m3x2_to_h2(wh0), e4m3x2_to_h2(wl0 >> 16), e4m3x2_to_h2(wh0 >> 16),
+                         qb[2 * ks], qb[2 * ks + 1]);
+        } else {
+          mma16816<false>(s, kr.pr[2 * ks], 0u, kr.pr[2 * ks + 1], 0u, qb[2 * ks], qb[2 * ks + 1]);
+        }
+      }
+      const bool ok = ri >= 0, okh = rih >= 0;
       // the next tile of the share (this unit or the next): its K rows now
       const bool next = w + 1 < w1;
       const int nri = e1 >= 0 ? e1 + g1 * P : -1;
-      e1 = load_entry(wl < w1);
+      const int nrih = e1h >= 0 ? e1h + g1 * P : -1;
+      e1 = load_entry(wl < w1, 0);
+      if constexpr (FP8) e1h = load_entry(wl < w1, 8);
       g1 = L.g;
       advance();
       ++wl;
-      if (next) kr.load(kbase + (size_t)max(nri, 0) * RR::kRowBytes, c4, nri >= 0);
-      // online softmax; s[0], s[1]: position gq, heads 2c4, 2c4 + 1
+      if (next) {
+        kr.load(kbase + (size_t)max(nri, 0) * RR::kRowBytes, c4, nri >= 0);
+        if constexpr (FP8) krh.load(kbase + (size_t)max(nrih, 0) * RR::kRowBytes, c4, nrih >= 0);
+      }
+      // online softmax; s[0], s[1]: position gq, heads 2c4, 2c4 + 1; s[2], s[3]:
+      // position gq + 8 (FP8 only)
       const float x0 = ok ? s[0] * scale_log2 : kNegInf;
       const float x1 = ok ? s[1] * scale_log2 : kNegInf;
-      float mA = x0, mB = x1;
+      const float x2 = FP8 && okh ? s[2] * scale_log2 : kNegInf;
+      const float x3 = FP8 && okh ? s[3] * scale_log2 : kNegInf;
+      float mA = fmaxf(x0, x2), mB = fmaxf(x1, x3);
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
         mA = fmaxf(mA, __shfl_xor_sync(kFull, mA, o));
@@ -316,8 +340,9 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const AttnArgs a) {
       const float bA = nA == kNegInf ? 0.f : nA, bB = nB == kNegInf ? 0.f : nB;
       const float alA = exp2f(m_run[0] - bA), alB = exp2f(m_run[1] - bB);
       const float p0 = exp2f(x0 - bA), p1 = exp2f(x1 - bB);
-      l_run[0] = l_run[0] * alA + p0;
-      l_run[1] = l_run[1] * alB + p1;
+      const float p2 = FP8 ? exp2f(x2 - bA) : 0.f, p3 = FP8 ? exp2f(x3 - bB) : 0.f;
+      l_run[0] = l_run[0] * alA + (p0 + p2);
+      l_run[1] = l_run[1] * alB + (p1 + p3);
       m_run[0] = nA;
       m_run[1] = nB;
 #pragma unroll
@@ -329,11 +354,25 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const AttnArgs a) {
       }
       // O^T += V^T P^T
       const uint32_t pb = movt(pack2<FP8>(p0, p1));
+      if constexpr (FP8) {
+        const uint32_t pbh = movt(pack2<true>(p2, p3));
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt)
-        mma16816<FP8>(acc[mt], movt(vr.pr[2 * mt]), movt(vr.pr[2 * mt + 1]), 0u, 0u, pb, 0u);
-      if (next) vr.load(vbase + (size_t)max(nri, 0) * RR::kRowBytes, c4, nri >= 0);
+        for (int mt = 0; mt < 8; ++mt) {
+          const uint32_t wl0 = vr.pr[mt], wh0 = vrh.pr[mt];
+          mma16816<true>(acc[mt], movt(e4m3x2_to_h2(wl0)), movt(e4m3x2_to_h2(wl0 >> 16)), movt(e4m3x2_to_h2(wh0)),
+                         movt(e4m3x2_to_h2(wh0 >> 16)), pb, pbh);
+        }
+      } else {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+          mma16816<false>(acc[mt], movt(vr.pr[2 * mt]), movt(vr.pr[2 * mt + 1]), 0u, 0u, pb, 0u);
+      }
+      if (next) {
+        vr.load(vbase + (size_t)max(nri, 0) * RR::kRowBytes, c4, nri >= 0);
+        if constexpr (FP8) vrh.load(vbase + (size_t)max(nrih, 0) * RR::kRowBytes, c4, nrih >= 0);
+      }
       ri = nri;
+      rih = nrih;
     }
 
     // ---- merge the 4 warps (the next unit's first K/V rows are in flight) ----
@@ -519,7 +558,8 @@ int page_shift_of(int page_size) {
 AttnPlan attn_plan(const qsa_dims& d, int num_sms) {
   AttnPlan pl;
   pl.units = d.batch * d.n_q * d.n_kv_heads;
-  pl.tiles = (d.width + kTile - 1) / kTile;
+  const int tile = d.kv_dtype == QSA_KV_FP8_E4M3 ? 64 : kTile;  // positions per CTA step (4 warps)
+  pl.tiles = (d.width + tile - 1) / tile;
   const long long total = (long long)pl.units * pl.tiles;
   const long long resident = 4LL * num_sms;  // 4 CTAs per SM
   pl.grid = (int)(total < resident ? total : resident);
