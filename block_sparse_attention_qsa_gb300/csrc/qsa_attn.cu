@@ -10,17 +10,16 @@
 // Design (stream-K). The (request, query, KV head) units times their tiles
 // of selected positions form one stream of tiles, cut into equal contiguous
 // shares, one per resident 4-warp CTA, so every CTA does the same work and
-// the kernel has no wave tail. Within a tile every warp works alone on 8
-// positions (BF16) or 16 (FP8, so that a step moves as many bytes). The
-// selected K/V rows are random 256-byte (BF16) or 128-byte (FP8) rows, so the
+// the kernel has no wave tail. Within a tile every warp works alone on 16
+// positions: lane 4g + c holds positions g and g + 8. The selected K/V rows are random 256-byte (BF16) or 128-byte (FP8) rows, so the
 // kernel is a gather: measured on GB300, 128-bit loads straight into
 // registers, with each warp reading whole rows, sustain a much higher share
 // of HBM bandwidth for such gathers than staging through shared memory. So K
 // and V never touch shared memory:
 //
 //  * S^T = K Q^T on the tensor cores (mma.sync m16n8k16, FP32 accumulate):
-//    the warp's positions are the M rows (BF16: rows 0..7, FP8: 0..15), the
-//    KV group's 8 query heads the N columns. A lane's 16-byte loads of K rows
+//    the warp's 16 positions are the M rows, the KV group's 8 query heads the
+//    N columns. A lane's 16-byte loads of K rows
 //    are its A fragments directly, because the head dim is visited in a
 //    lane-dependent order that Q's B fragments follow too (a dot product does
 //    not depend on the order of its terms).
@@ -45,7 +44,11 @@
 namespace qsa {
 namespace {
 
-constexpr int kTile = 32;       // BF16 positions per CTA step: 4 warps of 8 (FP8: 4 of 16)
+constexpr int kTile = 64;       // positions per CTA step: 4 warps of 16
+// resident CTAs per SM: BF16 rows take twice the registers of FP8 codes
+// (two rows of K and V per lane: 64 registers against 32)
+template <bool FP8>
+constexpr int kCtasPerSm = FP8 ? 4 : 3;
 constexpr int kThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -182,15 +185,15 @@ struct Cursor {
 };
 
 template <bool FP8>
-__global__ void __launch_bounds__(kThreads, 4) attn_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const AttnArgs a) {
   __shared__ __align__(16) __nv_bfloat16 sQ[2][kGroup * kDim];
   __shared__ __align__(16) float wacc[4 * kGroup * kDim];  // [warp][head][dim]
   __shared__ float s_ml[96];
   __shared__ int s_last;
 
-  // positions per warp step: 8 for BF16 (rows g of the mma), 16 for FP8
-  // (rows g and g + 8), so that an FP8 step moves as many bytes as a BF16 one
-  constexpr int POS = FP8 ? 16 : 8;
+  // 16 positions per warp step: lane 4g + c holds rows g and g + 8, all 16 M
+  // rows of the score mma and the full k of the PV mma
+  constexpr int POS = 16;
   constexpr int TILE = 4 * POS;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gq = lane >> 2, c4 = lane & 3;
@@ -237,21 +240,19 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const AttnArgs a) {
       }
     }
   };
-  const int e0 = load_entry(true, 0), e0h = FP8 ? load_entry(true, 8) : -1, g0 = L.g;
+  const int e0 = load_entry(true, 0), e0h = load_entry(true, 8), g0 = L.g;
   advance();
-  int e1 = load_entry(w0 + 1 < w1, 0), e1h = FP8 ? load_entry(w0 + 1 < w1, 8) : -1, g1 = L.g;
+  int e1 = load_entry(w0 + 1 < w1, 0), e1h = load_entry(w0 + 1 < w1, 8), g1 = L.g;
   advance();
   long long wl = w0 + 2;  // tile of the cursor
 
-  RR kr, vr, krh, vrh;  // krh, vrh: rows g + 8 (FP8 only)
+  RR kr, vr, krh, vrh;  // rows g and g + 8
   int ri = e0 >= 0 ? e0 + g0 * P : -1;
   int rih = e0h >= 0 ? e0h + g0 * P : -1;
   kr.load(kbase + (size_t)max(ri, 0) * RR::kRowBytes, c4, ri >= 0);
   vr.load(vbase + (size_t)max(ri, 0) * RR::kRowBytes, c4, ri >= 0);
-  if constexpr (FP8) {
-    krh.load(kbase + (size_t)max(rih, 0) * RR::kRowBytes, c4, rih >= 0);
-    vrh.load(vbase + (size_t)max(rih, 0) * RR::kRowBytes, c4, rih >= 0);
-  }
+  krh.load(kbase + (size_t)max(rih, 0) * RR::kRowBytes, c4, rih >= 0);
+  vrh.load(vbase + (size_t)max(rih, 0) * RR::kRowBytes, c4, rih >= 0);
 
   long long w = w0;
   for (int buf = 0;; buf ^= 1) {
@@ -307,7 +308,8 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const AttnArgs a) {
           mma16816<true>(s, e4m3x2_to_h2(wl0), e4m3x2_to_h2(wh0), e4m3x2_to_h2(wl0 >> 16), e4m3x2_to_h2(wh0 >> 16),
                          qb[2 * ks], qb[2 * ks + 1]);
         } else {
-          mma16816<false>(s, kr.pr[2 * ks], 0u, kr.pr[2 * ks + 1], 0u, qb[2 * ks], qb[2 * ks + 1]);
+          mma16816<false>(s, kr.pr[2 * ks], krh.pr[2 * ks], kr.pr[2 * ks + 1], krh.pr[2 * ks + 1], qb[2 * ks],
+                          qb[2 * ks + 1]);
         }
       }
       const bool ok = ri >= 0, okh = rih >= 0;
@@ -316,20 +318,20 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const AttnArgs a) {
       const int nri = e1 >= 0 ? e1 + g1 * P : -1;
       const int nrih = e1h >= 0 ? e1h + g1 * P : -1;
       e1 = load_entry(wl < w1, 0);
-      if constexpr (FP8) e1h = load_entry(wl < w1, 8);
+      e1h = load_entry(wl < w1, 8);
       g1 = L.g;
       advance();
       ++wl;
       if (next) {
         kr.load(kbase + (size_t)max(nri, 0) * RR::kRowBytes, c4, nri >= 0);
-        if constexpr (FP8) krh.load(kbase + (size_t)max(nrih, 0) * RR::kRowBytes, c4, nrih >= 0);
+        krh.load(kbase + (size_t)max(nrih, 0) * RR::kRowBytes, c4, nrih >= 0);
       }
       // online softmax; s[0], s[1]: position gq, heads 2c4, 2c4 + 1; s[2], s[3]:
-      // position gq + 8 (FP8 only)
+      // position gq + 8
       const float x0 = ok ? s[0] * scale_log2 : kNegInf;
       const float x1 = ok ? s[1] * scale_log2 : kNegInf;
-      const float x2 = FP8 && okh ? s[2] * scale_log2 : kNegInf;
-      const float x3 = FP8 && okh ? s[3] * scale_log2 : kNegInf;
+      const float x2 = okh ? s[2] * scale_log2 : kNegInf;
+      const float x3 = okh ? s[3] * scale_log2 : kNegInf;
       float mA = fmaxf(x0, x2), mB = fmaxf(x1, x3);
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
@@ -340,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const AttnArgs a) {
       const float bA = nA == kNegInf ? 0.f : nA, bB = nB == kNegInf ? 0.f : nB;
       const float alA = exp2f(m_run[0] - bA), alB = exp2f(m_run[1] - bB);
       const float p0 = exp2f(x0 - bA), p1 = exp2f(x1 - bB);
-      const float p2 = FP8 ? exp2f(x2 - bA) : 0.f, p3 = FP8 ? exp2f(x3 - bB) : 0.f;
+      const float p2 = exp2f(x2 - bA), p3 = exp2f(x3 - bB);
       l_run[0] = l_run[0] * alA + (p0 + p2);
       l_run[1] = l_run[1] * alB + (p1 + p3);
       m_run[0] = nA;
@@ -353,9 +355,8 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const AttnArgs a) {
         acc[k][3] *= alB;
       }
       // O^T += V^T P^T
-      const uint32_t pb = movt(pack2<FP8>(p0, p1));
+      const uint32_t pb = movt(pack2<FP8>(p0, p1)), pbh = movt(pack2<FP8>(p2, p3));
       if constexpr (FP8) {
-        const uint32_t pbh = movt(pack2<true>(p2, p3));
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
           const uint32_t wl0 = vr.pr[mt], wh0 = vrh.pr[mt];
@@ -365,11 +366,12 @@ __global__ void __launch_bounds__(kThreads, 4) attn_kernel(const AttnArgs a) {
       } else {
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt)
-          mma16816<false>(acc[mt], movt(vr.pr[2 * mt]), movt(vr.pr[2 * mt + 1]), 0u, 0u, pb, 0u);
+          mma16816<false>(acc[mt], movt(vr.pr[2 * mt]), movt(vr.pr[2 * mt + 1]), movt(vrh.pr[2 * mt]),
+                          movt(vrh.pr[2 * mt + 1]), pb, pbh);
       }
       if (next) {
         vr.load(vbase + (size_t)max(nri, 0) * RR::kRowBytes, c4, nri >= 0);
-        if constexpr (FP8) vrh.load(vbase + (size_t)max(nrih, 0) * RR::kRowBytes, c4, nrih >= 0);
+        vrh.load(vbase + (size_t)max(nrih, 0) * RR::kRowBytes, c4, nrih >= 0);
       }
       ri = nri;
       rih = nrih;
@@ -558,10 +560,10 @@ int page_shift_of(int page_size) {
 AttnPlan attn_plan(const qsa_dims& d, int num_sms) {
   AttnPlan pl;
   pl.units = d.batch * d.n_q * d.n_kv_heads;
-  const int tile = d.kv_dtype == QSA_KV_FP8_E4M3 ? 64 : kTile;  // positions per CTA step (4 warps)
-  pl.tiles = (d.width + tile - 1) / tile;
+  pl.tiles = (d.width + kTile - 1) / kTile;
   const long long total = (long long)pl.units * pl.tiles;
-  const long long resident = 4LL * num_sms;  // 4 CTAs per SM
+  const long long resident =
+      (long long)(d.kv_dtype == QSA_KV_FP8_E4M3 ? kCtasPerSm<true> : kCtasPerSm<false>) * num_sms;
   pl.grid = (int)(total < resident ? total : resident);
   return pl;
 }
