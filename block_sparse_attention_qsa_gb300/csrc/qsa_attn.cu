@@ -49,6 +49,11 @@ constexpr int kTile = 64;       // positions per CTA step: 4 warps of 16
 // (two rows of K and V per lane: 64 registers against 32)
 template <bool FP8>
 constexpr int kCtasPerSm = FP8 ? 4 : 3;
+// Small batches: each CTA takes at least this many tiles, so a unit is cut
+// into at most 17 pieces and the merge of the last piece to arrive stays short
+// (measured at batch 1: 1 tile 35.1 us per step, 2 tiles 32.2, 4 tiles 33.5).
+constexpr int kMinTilesPerCta = 2;
+constexpr int kMergeBatch = 4;  // pieces whose accumulators are read at once
 constexpr int kThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -459,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
       __syncthreads();
       if (s_last) {
         __threadfence();
-        // every piece's (max, sum) at once, then the accumulators 4 pieces at a time
+        // every piece's (max, sum) at once, then the accumulators kMergeBatch pieces at a time
         float* pm = wacc;                        // [n_piece][8] (the merge buffer is free now)
         float* pl = wacc + n_piece * kGroup;     // [n_piece][8]
         int* ps = reinterpret_cast<int*>(wacc + 2 * n_piece * kGroup);  // [n_piece] slots
@@ -486,17 +491,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
         __syncthreads();
 #pragma unroll
         for (int h = 0; h < 8; ++h) o[h] = 0.f;
-        for (int k0 = 0; k0 < n_piece; k0 += 4) {
-          float x[4][8];
+        for (int k0 = 0; k0 < n_piece; k0 += kMergeBatch) {
+          float x[kMergeBatch][8];  // 32 loads in flight per thread
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
+          for (int kk = 0; kk < kMergeBatch; ++kk) {
             const bool in = k0 + kk < n_piece;
             const float* pp = a.partials + (size_t)(in ? ps[k0 + kk] : 0) * kPartFloats + 2 * kGroup + tid;
 #pragma unroll
             for (int h = 0; h < 8; ++h) x[kk][h] = in ? __ldcg(pp + h * kDim) : 0.f;
           }
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
+          for (int kk = 0; kk < kMergeBatch; ++kk) {
             if (k0 + kk >= n_piece) break;
 #pragma unroll
             for (int h = 0; h < 8; ++h) o[h] += exp2f(pm[(k0 + kk) * kGroup + h] - sM[h]) * x[kk][h];
@@ -564,7 +569,8 @@ AttnPlan attn_plan(const qsa_dims& d, int num_sms) {
   const long long total = (long long)pl.units * pl.tiles;
   const long long resident =
       (long long)(d.kv_dtype == QSA_KV_FP8_E4M3 ? kCtasPerSm<true> : kCtasPerSm<false>) * num_sms;
-  pl.grid = (int)(total < resident ? total : resident);
+  const long long most = (total + kMinTilesPerCta - 1) / kMinTilesPerCta;
+  pl.grid = (int)(most < resident ? most : resident);
   return pl;
 }
 
