@@ -56,6 +56,9 @@ def parse_args():
     ap.add_argument("--no-flush", action="store_true", help="warm-L2 numbers (reported as such)")
     ap.add_argument("--step-only", action="store_true",
                     help="only the warm-up and timed fused steps (for profiler captures)")
+    ap.add_argument("--draft", action="store_true",
+                    help="time an MTP draft step instead: one draft query per request attending over the "
+                         "selection of the request's first verify query plus the 3 positions after it")
     return ap.parse_args()
 
 
@@ -305,6 +308,49 @@ def oracle_steps(spec, src, idx_keys_fn, n_steps=None, seconds=None):
     return tot_b, tot_s, done
 
 
+def run_draft(qsa, args, spec, st, sel_host, flush, stream, world, rank):
+    """MTP draft step reusing the step's selection (no scoring, no top-k):
+    per request one draft query at the last verify position, attending over
+    the first verify query's selection row plus the 3 positions after it."""
+    g = st["g"]
+    d = qsa.dims_for_spec(spec)
+    d.n_q = 1
+    ws = qsa.make_workspace(d)
+    qd = g["q"][:, :1].contiguous()
+    src = torch.zeros((spec.batch, 1), dtype=torch.int32, device="cuda")
+    p_draft = (g["q_pos"][:, :1] + 3).contiguous()
+    out = torch.empty((spec.batch, 1, spec.n_q_heads, spec.head_dim), dtype=torch.bfloat16, device="cuda")
+
+    def call():
+        qsa.draft_attn(d, qd, g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"], g["page_table"],
+                       st["sel_pos"], g["q_pos"], src, p_draft, out, ws)
+
+    call()
+    status, info = qsa.check_errors(ws)
+    if status != qsa.OK:
+        raise RuntimeError(f"device error during the draft step: {info}")
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_list = timed(call, args.steps, flush, stream)
+    barrier(world)
+    ms = max_over_ranks(sum(ms_list) / len(ms_list), world)
+    n_pos = sum(int((sel_host[r, 0] >= 0).sum()) + 3 for r in range(spec.batch))
+    b = n_pos * kv_row_bytes(spec) * 2  # K and V of each attended position, both KV heads
+    if rank == 0:
+        print(json.dumps({"metric": "QSA MTP draft-step attention over a reused selection", "workload": spec.name,
+                          "latency_us": round(ms * 1e3, 2),
+                          "latency_us_p10_p50_p90": [round(float(np.percentile(ms_list, q)) * 1e3, 2)
+                                                     for q in (10, 50, 90)],
+                          "value": round(b * world / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
+                          "bytes_per_step": int(b), "draft_queries_per_request": 1, "gap": 3,
+                          "l2": "no flush (warm)" if flush is None else "flushed before every step",
+                          "note": "entry-point time: positions resolved to cache rows, then attention"}))
+
+
 def run_ours(args, world, rank):
     qsa = build_lib()
     spec = synth.spec_for(args.config, batch=args.batch, ctx=args.ctx)
@@ -325,6 +371,8 @@ def run_ours(args, world, rank):
     b_kc = kc_bytes(spec)
     b_kv_union, b_kv_sum = kv_bytes(spec, sel_host)
     bytes_step = b_kc + b_kv_union
+    if args.draft:
+        return run_draft(qsa, args, spec, st, sel_host, flush, stream, world, rank)
 
     # warm-up, then exactly K timed steps
     for _ in range(args.warmup):

@@ -2,6 +2,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -24,12 +26,15 @@ WsLayout ws_layout(const qsa_dims& d, int num_sms) {
   w.units = pl.units;
   w.tiles = pl.tiles;
   w.grid = pl.grid;
+  qsa_dims dd = d;  // a draft step's wider selection may take more CTAs
+  dd.width = kDraftWidth;
+  const int grid_max = std::max(pl.grid, attn_plan(dd, num_sms).grid);
   const size_t rows = (size_t)d.batch * d.n_q;
   size_t off = 256;  // header
   w.tickets = off;
   off = align_up(off + (size_t)pl.units * sizeof(int32_t), 256);
   w.partials = off;
-  off = align_up(off + (size_t)pl.grid * 2 * kPartFloats * sizeof(float), 256);
+  off = align_up(off + (size_t)grid_max * 2 * kPartFloats * sizeof(float), 256);
   w.scores = off;
   off = align_up(off + rows * d.max_blocks * sizeof(float), 256);
   w.sel_blk = off;
@@ -37,7 +42,7 @@ WsLayout ws_layout(const qsa_dims& d, int num_sms) {
   w.sel_pos = off;
   off = align_up(off + rows * kWidth * sizeof(int32_t), 256);
   w.sel_row = off;
-  off = align_up(off + rows * kWidth * sizeof(int32_t), 256);
+  off = align_up(off + rows * kDraftWidth * sizeof(int32_t), 256);
   w.total = off;
   return w;
 }
@@ -226,6 +231,32 @@ qsa_status qsa_decode(const qsa_dims* dims, const void* q_idx, const void* kc, c
   e = launch_attn(*dims, q, k_cache, v_cache, k_scale, v_scale, srow, out, at<int32_t>(ws, w.tickets),
                   at<float>(ws, w.partials), pl, s, true);
   return from_cuda(e);
+}
+
+qsa_status qsa_draft_attn(const qsa_dims* dims, const void* q, const void* k_cache, const void* v_cache,
+                          const float* k_scale, const float* v_scale, const int32_t* page_table,
+                          const int32_t* sel_pos, const int32_t* sel_q_pos, int32_t n_sel, const int32_t* src,
+                          const int32_t* q_pos, void* out, void* ws, size_t ws_bytes, void* stream) {
+  qsa_status st = check_dims(dims);
+  if (st != QSA_OK) return st;
+  if (!q || !k_cache || !v_cache || !page_table || !sel_pos || !sel_q_pos || !src || !q_pos || !out)
+    return QSA_ERR_INVALID_ARG;
+  if (n_sel < 1 || n_sel > kMaxNq) return QSA_ERR_INVALID_ARG;
+  if (dims->kv_dtype == QSA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(q) & 3u))
+    return QSA_ERR_INVALID_ARG;
+  WsLayout w;
+  if ((st = check_ws(dims, ws, ws_bytes, &w)) != QSA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* srow = at<int32_t>(ws, w.sel_row);
+  if (launch_draft_resolve(*dims, sel_pos, sel_q_pos, n_sel, src, q_pos, page_table, srow, err_word(ws), s) !=
+      cudaSuccess)
+    return QSA_ERR_CUDA;
+  qsa_dims dd = *dims;  // attention over the widened selection
+  dd.width = kDraftWidth;
+  const AttnPlan pl = attn_plan(dd, device_sm_count());
+  return from_cuda(launch_attn(dd, q, k_cache, v_cache, k_scale, v_scale, srow, out, at<int32_t>(ws, w.tickets),
+                               at<float>(ws, w.partials), pl, s, true));
 }
 
 qsa_status qsa_check_errors(void* ws, void* stream, int32_t* info) {

@@ -554,6 +554,51 @@ __global__ void __launch_bounds__(256) resolve_kernel(const int32_t* __restrict_
   }
 }
 
+// Draft steps: row (r, j) of the widened selection = the reused row's
+// positions (checked against the row's own query position p_src), then
+// p_src + 1 .. p, as cache rows of KV head 0 (-1 for none).
+__global__ void __launch_bounds__(256) draft_resolve_kernel(const int32_t* __restrict__ sel_pos,
+                                                            const int32_t* __restrict__ sel_q_pos, int n_sel,
+                                                            const int32_t* __restrict__ src,
+                                                            const int32_t* __restrict__ q_pos,
+                                                            const int32_t* __restrict__ page_table,
+                                                            int32_t* __restrict__ sel_row, int32_t* err, int n_q,
+                                                            int n_kv, int page_shift, int max_pages, int num_pages) {
+  pdl_trigger();  // the attention kernel waits for this whole grid anyway
+  const int row = blockIdx.x, r = row / n_q, j = row - r * n_q;
+  const int sj = src[row];
+  const bool s_ok = sj >= 0 && sj < n_sel;
+  const int ps = s_ok ? sel_q_pos[r * n_sel + sj] : -1;
+  const int p = q_pos[row];
+  const bool ok = s_ok && ps >= 0 && p >= ps && p - ps <= kMaxDraftGap && (p >> page_shift) < max_pages;
+  if (!ok && threadIdx.x == 0) record_error(err, kErrDraft, r, j, s_ok ? p : sj);
+  const int page_mask = (1 << page_shift) - 1;
+  const int32_t* reused = sel_pos + ((size_t)r * n_sel + (s_ok ? sj : 0)) * kWidth;
+  for (int i = threadIdx.x; i < kDraftWidth; i += blockDim.x) {
+    int pos = -1;
+    if (ok) {
+      if (i < kWidth) {
+        pos = reused[i];
+        if (pos > ps) {
+          record_error(err, kErrSelPos, r, j, pos);
+          pos = -1;
+        }
+      } else if (i - kWidth < p - ps) {
+        pos = ps + 1 + (i - kWidth);
+      }
+    }
+    int ri = -1;
+    if (pos >= 0) {
+      const int page = page_table[(size_t)r * max_pages + (pos >> page_shift)];
+      if (page < 0 || page >= num_pages)
+        record_error(err, kErrPage, r, j, page);
+      else
+        ri = ((page * n_kv) << page_shift) + (pos & page_mask);
+    }
+    sel_row[(size_t)row * kDraftWidth + i] = ri;
+  }
+}
+
 int page_shift_of(int page_size) {
   int shift = 0;
   while ((1 << shift) < page_size) ++shift;
@@ -579,6 +624,14 @@ cudaError_t launch_resolve(const qsa_dims& d, const int32_t* sel_pos, const int3
   return launch_k(resolve_kernel, dim3(d.batch * d.n_q), dim3(256), 0, s, false, sel_pos, q_pos, page_table,
                   sel_row, err, d.n_q, d.n_kv_heads, page_shift_of(d.page_size), d.max_pages, d.num_pages,
                   d.width);
+}
+
+cudaError_t launch_draft_resolve(const qsa_dims& d, const int32_t* sel_pos, const int32_t* sel_q_pos, int n_sel,
+                                 const int32_t* src, const int32_t* q_pos, const int32_t* page_table,
+                                 int32_t* sel_row, int32_t* err, cudaStream_t s) {
+  return launch_k(draft_resolve_kernel, dim3(d.batch * d.n_q), dim3(256), 0, s, false, sel_pos, sel_q_pos, n_sel,
+                  src, q_pos, page_table, sel_row, err, d.n_q, d.n_kv_heads, page_shift_of(d.page_size),
+                  d.max_pages, d.num_pages);
 }
 
 cudaError_t launch_attn(const qsa_dims& d, const void* q, const void* k_cache, const void* v_cache,

@@ -20,7 +20,14 @@ constexpr int kGroup = 8;        // query heads per KV head
 constexpr int kMaxNq = 4;        // verify queries per request
 
 // Device error kinds recorded in the workspace header.
-enum DevErr : int32_t { kErrNone = 0, kErrQueryPos = 1, kErrPage = 2, kErrSelPos = 3, kErrTimeout = 5 };
+enum DevErr : int32_t {
+  kErrNone = 0, kErrQueryPos = 1, kErrPage = 2, kErrSelPos = 3, kErrDraft = 4, kErrTimeout = 5
+};
+
+// Draft-step reuse: a draft query attends over a reused selection row plus at
+// most kMaxDraftGap positions after the row's own query.
+constexpr int kMaxDraftGap = QSA_MAX_DRAFT_GAP;
+constexpr int kDraftWidth = kWidth + kMaxDraftGap;
 
 // ---------------------------------------------------------------------------
 // Workspace layout (byte offsets from the 256-aligned base).
@@ -30,7 +37,8 @@ enum DevErr : int32_t { kErrNone = 0, kErrQueryPos = 1, kErrPage = 2, kErrSelPos
 //   scores (decode)    float [B][n_q][max_blocks]
 //   sel_blk (decode)   int32 [B][n_q][512]
 //   sel_pos (decode)   int32 [B][n_q][2051]
-//   sel_row            int32 [B][n_q][2051]    cache row (KV head 0) of each selected position
+//   sel_row            int32 [B][n_q][2051 + kMaxDraftGap]  cache row (KV head 0) of each
+//                      selected position (row stride 2051, or 2051 + kMaxDraftGap for draft steps)
 // ---------------------------------------------------------------------------
 constexpr int kPartFloats = 2 * kGroup + kGroup * kDim;  // m[8], l[8], acc[8][128]
 
@@ -114,6 +122,10 @@ cudaError_t launch_score(const qsa_dims& d, const __nv_bfloat16* q_idx, const __
 cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q_pos,
                         int32_t* sel_blk, int32_t* sel_pos, int32_t* err, const int32_t* page_table,
                         int32_t* sel_row, cudaStream_t s, bool pdl);
+// draft step: reused selection rows plus the positions since -> cache rows
+cudaError_t launch_draft_resolve(const qsa_dims& d, const int32_t* sel_pos, const int32_t* sel_q_pos, int n_sel,
+                                 const int32_t* src, const int32_t* q_pos, const int32_t* page_table,
+                                 int32_t* sel_row, int32_t* err, cudaStream_t s);
 // selected positions -> cache rows (KV head 0) with all index checks
 cudaError_t launch_resolve(const qsa_dims& d, const int32_t* sel_pos, const int32_t* q_pos,
                            const int32_t* page_table, int32_t* sel_row, int32_t* err, cudaStream_t s);

@@ -31,8 +31,10 @@ BLOCK, TOPK, WIDTH = 4, 512, 2051
 EXPORTS = (
     "qsa_abi_version", "qsa_status_str", "qsa_dims_default", "qsa_workspace_size",
     "qsa_workspace_init", "qsa_compress_keys", "qsa_score", "qsa_topk", "qsa_sparse_attn",
-    "qsa_decode", "qsa_check_errors", "qsa_sparse_attn_noalloc",
+    "qsa_decode", "qsa_check_errors", "qsa_sparse_attn_noalloc", "qsa_draft_attn",
 )
+
+MAX_DRAFT_GAP = 64  # QSA_MAX_DRAFT_GAP
 
 
 class QSAError(RuntimeError):
@@ -74,6 +76,7 @@ def _load() -> ctypes.CDLL:
         "qsa_decode": (I, [D, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "qsa_check_errors": (I, [P, P, ctypes.POINTER(ctypes.c_int32)]),
         "qsa_sparse_attn_noalloc": (I, [D, P, P, P, P, P, P, P, P, P, P]),
+        "qsa_draft_attn": (I, [D, P, P, P, P, P, P, P, P, ctypes.c_int32, P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -230,6 +233,25 @@ def sparse_attn_noalloc(d: Dims, q, k_cache, v_cache, k_scale, v_scale, page_tab
     _check(lib.qsa_sparse_attn_noalloc(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                        _ptr(v_scale), _ptr(page_table), _ptr(sel_pos), _ptr(q_pos), _ptr(out),
                                        _stream(stream)), "qsa_sparse_attn_noalloc")
+
+
+def draft_attn(d: Dims, q, k_cache, v_cache, k_scale, v_scale, page_table, sel_pos, sel_q_pos, src, q_pos,
+               out, ws, stream=None):
+    """MTP draft step reusing an earlier selection: draft query j of request r
+    (d.n_q draft queries per request) attends over row src[r][j] of sel_pos
+    (made for a query at sel_q_pos[r][src[r][j]]) plus the positions after
+    that query up to its own, q_pos[r][j]."""
+    _check_attn_inputs(d, q, k_cache, v_cache, k_scale, v_scale, page_table, q_pos, out)
+    if sel_pos.dim() != 3 or sel_pos.shape[0] != d.batch or sel_pos.shape[2] != d.width:
+        raise ValueError(f"sel_pos: expected [{d.batch}][n_sel][{d.width}], got {tuple(sel_pos.shape)}")
+    n_sel = int(sel_pos.shape[1])
+    _want(sel_pos, "sel_pos", (d.batch, n_sel, d.width), torch.int32)
+    _want(sel_q_pos, "sel_q_pos", (d.batch, n_sel), torch.int32)
+    _want(src, "src", (d.batch, d.n_q), torch.int32)
+    w, n = _ws(d, ws)
+    _check(lib.qsa_draft_attn(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                              _ptr(page_table), _ptr(sel_pos), _ptr(sel_q_pos), n_sel, _ptr(src), _ptr(q_pos),
+                              _ptr(out), w, n, _stream(stream)), "qsa_draft_attn")
 
 
 def decode(d: Dims, q_idx, kc, q, k_cache, v_cache, k_scale, v_scale, page_table, q_pos, out, ws,

@@ -81,6 +81,10 @@ extern "C" {
 
 #define QSA_ABI_VERSION 1
 
+/* Most positions a draft query may lie after the query whose selection it
+ * reuses (qsa_draft_attn). */
+#define QSA_MAX_DRAFT_GAP 64
+
 typedef enum {
   QSA_OK = 0,
   QSA_ERR_INVALID_ARG = 1, /* null pointer, bad size or stride */
@@ -207,11 +211,33 @@ qsa_status qsa_sparse_attn_noalloc(const qsa_dims* dims, const void* q, const vo
                                    const int32_t* page_table, const int32_t* sel_pos,
                                    const int32_t* q_pos, void* out, void* stream);
 
+/* MTP draft steps reusing an earlier selection (arex-research.com, section
+ * "四类优化" heading: "MTP 复用"; 10100.com, "第三处": later draft steps reuse
+ * the attention positions selected before, instead of scoring and selecting
+ * again). Scoring and top-k are skipped; only attention runs. dims describes
+ * the draft step: batch, n_q = draft queries per request (1..4), heads and
+ * cache as for qsa_sparse_attn, width 2,051. sel_pos [B][n_sel][2051] holds
+ * selection rows made by qsa_topk / qsa_decode for queries at positions
+ * sel_q_pos [B][n_sel] (n_sel 1..4). Draft query j of request r, at position
+ * p = q_pos[r][j], reuses row src[r][j] (0 <= src < n_sel), made for
+ * p_src = sel_q_pos[r][src[r][j]]: out[r][j] = softmax(sm_scale q K^T) V over
+ * the valid positions of that row plus every position p_src + 1 .. p, which
+ * the row cannot hold (p_src <= p <= p_src + QSA_MAX_DRAFT_GAP). A draft
+ * query outside that range (or a bad src) is reported (kind 4) and gets a
+ * zero output; bad pages and selected positions after p_src are reported and
+ * skipped as in qsa_sparse_attn. The workspace is sized by
+ * qsa_workspace_size for dims. */
+qsa_status qsa_draft_attn(const qsa_dims* dims, const void* q, const void* k_cache, const void* v_cache,
+                          const float* k_scale, const float* v_scale, const int32_t* page_table,
+                          const int32_t* sel_pos, const int32_t* sel_q_pos, int32_t n_sel, const int32_t* src,
+                          const int32_t* q_pos, void* out, void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronises `stream`, reads and clears the device error record in `ws`.
  * Returns QSA_OK if no device-side error was recorded since the last check,
  * else QSA_ERR_BAD_INDEX (or QSA_ERR_TIMEOUT). `info` (may be NULL) receives
- * 4 int32: error kind (1 query position, 2 page id, 3 selected position),
- * request, query, offending value. */
+ * 4 int32: error kind (1 query position, 2 page id, 3 selected position,
+ * 4 draft query not after its reused selection), request, query, offending
+ * value. */
 qsa_status qsa_check_errors(void* ws, void* stream, int32_t* info);
 
 #ifdef __cplusplus

@@ -32,7 +32,12 @@ reason in the design notes of the repository):
     positions, then the partial block's positions, then -1 up to 2,051;
   * attention: query head h reads KV head h // (H_q / H_kv); scale
     1/sqrt(head_dim); plain max-subtracted softmax over the valid selected
-    positions; FP8 values are decode(code) * per-head FP32 scale.
+    positions; FP8 values are decode(code) * per-head FP32 scale;
+  * MTP draft steps (arex, same section, heading "MTP 复用"; 10100.com,
+    "第三处": later draft steps reuse the positions selected before): a draft
+    query at p reusing the selection row made for a query at p_src <= p
+    attends over that row's positions plus p_src + 1 .. p, the positions the
+    row cannot hold (at most 64 of them).
 
 All floating point here is FP64 unless a step fixes FP32 (the score buffer,
 the compressed-key mean) or BF16 (the compressed key's storage).
@@ -48,6 +53,7 @@ import numpy as np
 BLOCK = 4
 TOPK = 512
 WIDTH = TOPK * BLOCK + (BLOCK - 1)  # 2,051
+MAX_DRAFT_GAP = 64  # positions a draft query may lie after the selection's query
 
 
 # ---------------------------------------------------------------------------
@@ -226,6 +232,28 @@ def sparse_attn(q_bits: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
             w = np.exp(s - s.max())
             out[h] = (w @ V) / w.sum()
     return out
+
+
+def draft_positions(sel_row: np.ndarray, p_src: int, p: int) -> np.ndarray:
+    """Positions a draft query at p attends to when it reuses the selection
+    row ``sel_row`` made for a query at p_src (arex, "四类优化", MTP reuse;
+    10100.com, "第三处"): the row's valid positions, then p_src + 1 .. p."""
+    if not (0 <= p_src <= p <= p_src + MAX_DRAFT_GAP):
+        raise ValueError(f"draft position {p} does not follow its selection's query {p_src}")
+    kept = [int(t) for t in sel_row if t >= 0]
+    if any(t > p_src for t in kept):
+        raise ValueError("selection row holds a position after its own query")
+    return np.array(kept + list(range(p_src + 1, p + 1)), dtype=np.int64)
+
+
+def draft_attn(q_bits: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, page_table_row: np.ndarray,
+               sel_row: np.ndarray, p_src: int, p: int, kv_dtype: str = "bf16",
+               k_scale: Optional[Sequence[float]] = None, v_scale: Optional[Sequence[float]] = None,
+               sm_scale: Optional[float] = None) -> np.ndarray:
+    """Attention of a draft query at p over a reused selection row (made for
+    p_src) and the positions after p_src, FP64 [H_q][D]."""
+    return sparse_attn(q_bits, k_cache, v_cache, page_table_row, draft_positions(sel_row, p_src, p), kv_dtype,
+                       k_scale, v_scale, sm_scale)
 
 
 def dense_attn(q: np.ndarray, K: np.ndarray, V: np.ndarray, allowed: Sequence[int],

@@ -28,11 +28,17 @@ def _declared():
 
 def test_exports_every_declared_symbol(qsa):
     names = _declared()
-    assert len(names) == 12
+    assert len(names) == 13
     assert set(names) == set(qsa.EXPORTS)
     lib = ctypes.CDLL(qsa.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
+
+
+def test_draft_gap_matches_the_header(qsa):
+    txt = open(os.path.join(ROOT, "include", "qsa.h")).read()
+    m = re.search(r"#define QSA_MAX_DRAFT_GAP (\d+)", txt)
+    assert m and int(m.group(1)) == qsa.MAX_DRAFT_GAP
 
 
 def test_abi_version_and_status_strings(qsa):

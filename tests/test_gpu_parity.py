@@ -393,6 +393,93 @@ def _run_decode(qsa, spec, g):
     return out, sp
 
 
+# --------------------------------------------------------------------------
+# MTP draft steps reusing an earlier selection (qsa_draft_attn)
+# --------------------------------------------------------------------------
+
+def _draft_case(qsa, spec, g, q_sel, src, p_draft):
+    """Selections of verify queries at q_sel (through qsa_decode), then draft
+    queries at p_draft reusing rows src of them. Returns (out, sel_pos)."""
+    gs = dict(g)
+    gs["q_pos"] = torch.tensor(q_sel, dtype=torch.int32, device="cuda")
+    _, sp = _run_decode(qsa, spec, gs)
+    n_d = len(src[0])
+    d = qsa.dims_for_spec(spec)
+    d.n_q = n_d
+    ws = qsa.make_workspace(d)
+    qd = g["q"][:, :n_d].contiguous()
+    out = torch.full((spec.batch, n_d, 16, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    qsa.draft_attn(d, qd, g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"], g["page_table"], sp,
+                   gs["q_pos"], torch.tensor(src, dtype=torch.int32, device="cuda"),
+                   torch.tensor(p_draft, dtype=torch.int32, device="cuda"), out, ws)
+    return out, sp, ws
+
+
+def _draft_ref(npi, spec, sp, q_sel, src, p_draft, r, jd):
+    s = src[r][jd]
+    ks = npi["k_scale"] if spec.kv_dtype == "fp8" else None
+    vs = npi["v_scale"] if spec.kv_dtype == "fp8" else None
+    return O.draft_attn(npi["q"][r, jd], npi["k_cache"], npi["v_cache"], npi["page_table"][r], sp[r, s],
+                        q_sel[r][s], p_draft[r][jd], spec.kv_dtype, ks, vs)
+
+
+@pytest.mark.parametrize("name", ["b2-h1-bf16", "b2-nq2-h1-fp8", "b2-nq3-h3"])
+def test_draft_attn_parity(qsa, name):
+    spec = SPECS[name]()
+    inp = synth.make_inputs(spec)
+    npi = to_numpy_inputs(inp)
+    g = _dev(inp)
+    # verify queries 70 positions before the cache's end leave room for drafts
+    q_sel = [[p - 70 for p in row] for row in spec.q_pos()]
+    last = spec.n_q - 1
+    src = [[last, 0] for _ in range(spec.batch)]
+    p_draft = [[row[last] + 60, row[0] + 5] for row in q_sel]  # gaps of 60 and 5
+    out, sp, ws = _draft_case(qsa, spec, g, q_sel, src, p_draft)
+    _check_ok(qsa, ws)
+    got = out.float().cpu().numpy()
+    spn = sp.cpu().numpy()
+    for r in range(spec.batch):
+        for jd in range(2):
+            ref = _draft_ref(npi, spec, spn, q_sel, src, p_draft, r, jd)
+            err = np.max(np.abs(got[r, jd] - ref))
+            assert err <= ATOL[spec.kv_dtype], (r, jd, err)
+
+
+def test_draft_attn_full_size_sampled(qsa):
+    spec = synth.spec_for(2)
+    inp = synth.make_inputs(spec)
+    g = _dev(inp)
+    q_sel = spec.q_pos()
+    src = [[0] for _ in range(spec.batch)]
+    p_draft = [[row[0] + 3] for row in q_sel]  # the step's last verify position, from the first one's selection
+    out, sp, ws = _draft_case(qsa, spec, g, q_sel, src, p_draft)
+    _check_ok(qsa, ws)
+    got = out.float().cpu().numpy()
+    spn = sp.cpu().numpy()
+    npi = to_numpy_inputs({k: inp[k] for k in ("q", "k_cache", "v_cache", "k_scale", "v_scale", "page_table")})
+    for r in (0, 13, 31):
+        ref = _draft_ref(npi, spec, spn, q_sel, src, p_draft, r, 0)
+        err = np.max(np.abs(got[r, 0] - ref))
+        assert err <= ATOL["bf16"], (r, err)
+
+
+def test_draft_attn_reports_a_draft_before_its_selection(qsa):
+    spec = SPECS["b2-h1-bf16"]()
+    inp = synth.make_inputs(spec)
+    npi = to_numpy_inputs(inp)
+    g = _dev(inp)
+    q_sel = [[p - 70 for p in row] for row in spec.q_pos()]
+    src = [[1], [0]]
+    p_draft = [[q_sel[0][1] - 1], [q_sel[1][0] + 2]]  # request 0's draft lies before its selection's query
+    out, sp, ws = _draft_case(qsa, spec, g, q_sel, src, p_draft)
+    st, info = qsa.check_errors(ws)
+    assert st == qsa.ERR_BAD_INDEX and info[0] == 4 and info[1] == 0, info
+    got = out.float().cpu().numpy()
+    assert np.all(got[0, 0] == 0.0)  # the bad row attends over nothing
+    ref = _draft_ref(npi, spec, sp.cpu().numpy(), q_sel, src, p_draft, 1, 0)
+    assert np.max(np.abs(got[1, 0] - ref)) <= ATOL["bf16"]
+
+
 def test_decode_repeats_bit_exactly_on_one_workspace(qsa):
     # the workspace's counters and histograms must be left clean by every call
     spec = small_spec([9000, 3001, 5000], n_q=4, seed=36)

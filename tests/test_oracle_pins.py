@@ -358,6 +358,76 @@ def test_each_verify_query_sees_only_its_prefix():
                 assert not np.array_equal(res["out"][(0, jj)], base["out"][(0, jj)])
 
 
+# --------------------------------------------------------------------------
+# MTP draft steps reusing a selection (arex "四类优化", MTP reuse; 10100 第三处)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_draft_equals_dense_when_everything_fits(kv):
+    # 1,500 + 4 tokens: the selection of the query at 1,500 holds every position
+    # 0..1500, so a draft query at 1,503 reusing it sees exactly 0..1503
+    spec = small_spec([1500], n_q=4, kv_dtype=kv, seed=71)
+    npi = _oracle_inputs(spec)
+    res = O.decode_step(npi, kv, rows=[(0, 0)])
+    row = res["sel_pos"][(0, 0)]
+    q = npi["q"][0, 3]
+    ks = npi["k_scale"] if kv == "fp8" else None
+    vs = npi["v_scale"] if kv == "fp8" else None
+    out = O.draft_attn(q, npi["k_cache"], npi["v_cache"], npi["page_table"][0], row, 1500, 1503, kv, ks, vs)
+    dense = _dense_for(npi, spec, 0, 3, list(range(1504)))
+    assert np.max(np.abs(out - dense)) < 1e-12
+
+
+def test_draft_beyond_512_blocks_is_the_row_plus_the_gap():
+    spec = small_spec([3001], n_q=4, seed=72)
+    npi = _oracle_inputs(spec)
+    res = O.decode_step(npi, rows=[(0, 0)])
+    row = res["sel_pos"][(0, 0)]
+    assert _valid(row) == 2050  # 512 blocks + the unfilled block: 3,002 tokens = 4 * 750 + 2
+    allowed = sorted(set(int(t) for t in row if t >= 0) | {3002, 3003, 3004})
+    assert len(allowed) == 2053
+    out = O.draft_attn(npi["q"][0, 3], npi["k_cache"], npi["v_cache"], npi["page_table"][0], row, 3001, 3004)
+    dense = _dense_for(npi, spec, 0, 3, allowed)
+    assert np.max(np.abs(out - dense)) < 1e-12
+    # with no gap the draft query attends over the row alone
+    out0 = O.draft_attn(npi["q"][0, 3], npi["k_cache"], npi["v_cache"], npi["page_table"][0], row, 3001, 3001)
+    dense0 = _dense_for(npi, spec, 0, 3, sorted(int(t) for t in row if t >= 0))
+    assert np.max(np.abs(out0 - dense0)) < 1e-12
+
+
+def test_draft_position_bounds():
+    row = np.full(2051, -1, np.int32)
+    row[:3] = [0, 1, 2]
+    assert O.draft_positions(row, 10, 10).tolist() == [0, 1, 2]
+    assert O.draft_positions(row, 10, 13).tolist() == [0, 1, 2, 11, 12, 13]
+    assert len(O.draft_positions(row, 10, 10 + O.MAX_DRAFT_GAP)) == 3 + O.MAX_DRAFT_GAP
+    with pytest.raises(ValueError):
+        O.draft_positions(row, 10, 9)  # before its selection's query
+    with pytest.raises(ValueError):
+        O.draft_positions(row, 10, 11 + O.MAX_DRAFT_GAP)  # too far after it
+    bad = row.copy()
+    bad[3] = 11
+    with pytest.raises(ValueError):
+        O.draft_positions(bad, 10, 12)  # a reused row may not hold a later position
+
+
+def test_draft_is_causal():
+    spec = small_spec([2600], n_q=4, seed=73)
+    npi = _oracle_inputs(spec)
+    row = O.decode_step(npi, rows=[(0, 0)])["sel_pos"][(0, 0)]
+    args = (npi["q"][0, 2], npi["page_table"][0], row, 2600, 2602)
+    base = O.draft_attn(args[0], npi["k_cache"], npi["v_cache"], *args[1:])
+    P = spec.page_size
+    kc, vc = npi["k_cache"].copy(), npi["v_cache"].copy()
+    page = npi["page_table"][0, 2603 // P]
+    kc[page, :, 2603 % P] ^= np.uint16(0x0013)  # after the draft query: no effect
+    vc[page, :, 2603 % P] ^= np.uint16(0x000F)
+    assert np.array_equal(O.draft_attn(args[0], kc, vc, *args[1:]), base)
+    page = npi["page_table"][0, 2602 // P]
+    vc[page, :, 2602 % P] ^= np.uint16(0x000F)  # in the gap: the output moves
+    assert not np.array_equal(O.draft_attn(args[0], kc, vc, *args[1:]), base)
+
+
 def test_attention_softmax_invariants():
     spec = small_spec([700], n_q=1, seed=61)
     npi = _oracle_inputs(spec)
