@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(cons
   constexpr int STEPS = Geo::STEPS, PD = Geo::PD;
   constexpr int CPB = H * 16;  // 16-B chunks per block row
   extern __shared__ int s_off[];  // [B + 1] first unit (16 blocks) of each request
+  int* s_nb = s_off + B + 1;      // [B] full blocks of each request (its longest query)
 
   pdl_wait();  // no-op unless launched as a dependent
   // Let the selector launch now: its CTAs take each SM as this kernel's CTA
@@ -146,9 +147,14 @@ __global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(cons
       const int r = base + lane;
       int units = 0;
       if (r < B) {
+        int pv[kMaxNq];  // all of the request's positions in flight at once
+#pragma unroll
+        for (int j = 0; j < kMaxNq; ++j) pv[j] = j < n_q ? q_pos[r * n_q + j] : 0;
         int nb = 0;
-        for (int j = 0; j < n_q; ++j) {
-          const int p = q_pos[r * n_q + j];
+#pragma unroll
+        for (int j = 0; j < kMaxNq; ++j) {
+          if (j >= n_q) break;
+          const int p = pv[j];
           if (p < 0 || n_full_of(p) > max_blocks) {
             if (blockIdx.x == 0) record_error(err, kErrQueryPos, r, j, p);
           } else {
@@ -156,6 +162,7 @@ __global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(cons
           }
         }
         units = (nb + 15) / 16;
+        s_nb[r] = nb;
       }
       int v = units;
 #pragma unroll
@@ -191,27 +198,23 @@ __global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(cons
 
     // B fragments: query g (zero past n_q), dims 8c..8c+7 of every 32-dim chunk
     uint4 qf[STEPS];
-    int nbq[kMaxNq];
-    int nb_r = 0;
-#pragma unroll
-    for (int j = 0; j < kMaxNq; ++j) {
-      int p = -1;
-      if (j < n_q) p = q_pos[r * n_q + j];
-      const bool ok = p >= 0 && n_full_of(p) <= max_blocks;
-      nbq[j] = ok ? n_full_of(p) : 0;
-      nb_r = max(nb_r, nbq[j]);
-    }
+    const int nb_r = s_nb[r];  // bounds this request's key loads without waiting for q_pos
     {
       const uint4* qrow = reinterpret_cast<const uint4*>(q_idx + (size_t)(r * n_q + (g < n_q ? g : 0)) * CPB * 8);
 #pragma unroll
       for (int s = 0; s < STEPS; ++s) qf[s] = (g < n_q) ? qrow[s * 4 + c] : make_uint4(0, 0, 0, 0);
     }
-    // this lane stores queries 2c, 2c+1 (lanes with c < 2)
+    // this lane stores queries 2c, 2c+1 (lanes with c < 2); needed only at the stores
     int nb0 = 0, nb1 = 0;
-#pragma unroll
-    for (int j = 0; j < kMaxNq; ++j) {
-      nb0 = (j == 2 * c) ? nbq[j] : nb0;
-      nb1 = (j == 2 * c + 1) ? nbq[j] : nb1;
+    if (c < 2) {
+      if (2 * c < n_q) {
+        const int p = q_pos[r * n_q + 2 * c];
+        nb0 = (p >= 0 && n_full_of(p) <= max_blocks) ? n_full_of(p) : 0;
+      }
+      if (2 * c + 1 < n_q) {
+        const int p = q_pos[r * n_q + 2 * c + 1];
+        nb1 = (p >= 0 && n_full_of(p) <= max_blocks) ? n_full_of(p) : 0;
+      }
     }
     const uint4* kc_r = kc + (size_t)r * max_blocks * CPB;
     float* sc_r = scores + (size_t)r * n_q * max_blocks;
@@ -259,7 +262,7 @@ cudaError_t launch_score_h(const qsa_dims& d, const __nv_bfloat16* q_idx, const 
                            const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s,
                            bool pdl) {
   auto kern = score_kernel<H>;
-  const size_t smem = (size_t)(d.batch + 1) * sizeof(int);
+  const size_t smem = (size_t)(2 * d.batch + 1) * sizeof(int);
   static int occ_cache[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
