@@ -34,6 +34,7 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kKpt = 24;         // most keys per thread on the register path
+constexpr int kMaxCluster = 8;   // CTAs per row for small batches (portable cluster size)
 constexpr int kFastCap = kKpt * kThreads - 4;  // longest row on it (3 blocks of alignment slack)
 constexpr int kKeyCap = 49152;   // keys cached in shared memory on the long-row path
 constexpr int kPtCap = 4096;     // page-table entries staged in shared memory
@@ -421,6 +422,237 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Small batches: a thread-block cluster of C CTAs per row. CTA k of the
+// cluster keeps the keys of blocks [n k / C, n (k+1) / C) in registers (a
+// contiguous run of at most KPT per thread); each radix digit's histogram is
+// counted per CTA and summed through distributed shared memory between
+// cluster barriers; a cluster-level prefix of the per-CTA counts gives every
+// CTA the global slots of its picks, which it writes directly. The hardware
+// cluster barrier is the only wait.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// address of `p` (this CTA's shared memory) in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+  return a;
+}
+__device__ __forceinline__ uint32_t ld_peer(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+constexpr int kClHdrWords = 2048 + 2048 + 2048 + 64 + 8 + 8 + kPtCap;  // hist, hist2, sum, wsum, res, cnt, pt
+
+template <int KPT>
+__global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const float* __restrict__ scores,
+                                                                   const int32_t* __restrict__ q_pos,
+                                                                   int32_t* __restrict__ sel_blk,
+                                                                   int32_t* __restrict__ sel_pos, int32_t* err,
+                                                                   const RowOut ro, int n_q, int max_blocks) {
+  extern __shared__ __align__(16) uint32_t sm[];
+  uint32_t* hist = sm;             // [2048] this CTA's digit-1 (then digit-3) counts
+  uint32_t* hist2 = hist + 2048;   // [2048] this CTA's digit-2 counts
+  uint32_t* gsum = hist2 + 2048;   // [2048] the cluster's sums
+  uint32_t* wsum = gsum + 2048;    // [2][32]
+  int* res = reinterpret_cast<int*>(wsum + 64);  // [8]
+  uint32_t* cnt = wsum + 64 + 8;   // [8]: this CTA's selected and tied counts
+  int32_t* pt_s = reinterpret_cast<int32_t*>(cnt + 8);
+  const int tid = threadIdx.x;
+  const uint32_t crank = cluster_rank(), C = cluster_size();
+  const int row = blockIdx.x / (int)C;
+  const int r = row / n_q, j = row - r * n_q;
+
+  // inputs that do not come from the score kernel
+  const int p = q_pos[row];
+  bool pt_ok = false;
+  if (ro.page_table && p >= 0) {
+    const int pages = min((p >> ro.page_shift) + 1, ro.max_pages);
+    if (pages <= kPtCap) {
+      pt_ok = true;
+      for (int i = tid; i < pages; i += kThreads) pt_s[i] = ro.page_table[(size_t)r * ro.max_pages + i];
+    }
+  }
+  for (int i = tid; i < 4096; i += kThreads) hist[i] = 0;  // hist and hist2
+  pdl_wait();  // the scores come from the previous kernel
+  pdl_trigger();
+  __syncthreads();
+
+  int32_t* ob = sel_blk + (size_t)row * kTopK;
+  int32_t* op = sel_pos + (size_t)row * kWidth;
+  int32_t* orow = ro.page_table ? ro.sel_row + (size_t)row * kWidth : nullptr;
+  const int32_t* pt = pt_ok ? pt_s : nullptr;
+  const bool p_ok = p >= 0 && n_full_of(p) <= max_blocks && (!orow || (p >> ro.page_shift) < ro.max_pages);
+  const int n = p_ok ? n_full_of(p) : 0;
+  if (!p_ok || n <= kTopK) {
+    if (crank == 0) {
+      if (!p_ok && tid == 0) record_error(err, kErrQueryPos, r, j, p);
+      for (int i = tid; i < kTopK; i += kThreads) ob[i] = i < n ? i : -1;
+      for (int i = tid; i < kWidth; i += kThreads) op[i] = (p_ok && i <= p) ? i : -1;
+      if (orow)
+        for (int i = tid; i < kWidth; i += kThreads) orow[i] = (p_ok && i <= p) ? row_of(ro, pt, r, i, err, j) : -1;
+    }
+    cluster_sync();
+    return;
+  }
+  const int npart = (p + 1) & 3;
+  const float* srow = scores + (size_t)row * max_blocks;
+  const int b0 = (int)((long long)n * crank / C), b1 = (int)((long long)n * (crank + 1) / C);
+  const int v0 = b0 + tid * KPT;
+  const int cnt_here = min(KPT, max(0, b1 - v0));
+  constexpr uint32_t kAll = KPT >= 32 ? 0xffffffffu : (1u << KPT) - 1u;
+  const uint32_t valid_m = cnt_here >= KPT ? kAll : ((1u << cnt_here) - 1u);
+
+  // the cluster's sum of a per-CTA histogram, into gsum
+  auto cluster_sum = [&](const uint32_t* local, int nbins) {
+    for (int i = tid; i < nbins; i += kThreads) {
+      uint32_t acc = 0;
+      for (uint32_t k = 0; k < C; ++k) acc += ld_peer(peer_addr(local + i, k));
+      gsum[i] = acc;
+    }
+    __syncthreads();
+  };
+
+  // pass 1: keys into registers, this CTA's histogram of the top 11 bits
+  uint32_t key[KPT];
+#pragma unroll
+  for (int e = 0; e < KPT; ++e) key[e] = ((valid_m >> e) & 1u) ? order_key(srow[v0 + e]) : 0u;
+#pragma unroll
+  for (int e = 0; e < KPT; ++e)
+    if ((valid_m >> e) & 1u) atomicAdd(&hist[key[e] >> 21], 1u);
+  cluster_sync();
+  cluster_sum(hist, 2048);
+  uint32_t need = kTopK;
+  find_bin<2048>(gsum, need, wsum, res);
+  const uint32_t d1 = (uint32_t)res[0];
+  need -= (uint32_t)res[1];
+
+  // pass 2: above the threshold bin / in it; digit 2 of the latter
+  const uint32_t lo_key = d1 << 21;
+  const uint32_t hi_key = d1 == 2047u ? 0xffffffffu : ((d1 + 1u) << 21) - 1u;
+  uint32_t gt_m = 0, eq_m = 0;
+#pragma unroll
+  for (int e = 0; e < KPT; ++e) {
+    gt_m |= (uint32_t)(key[e] > hi_key) << e;
+    eq_m |= (uint32_t)(key[e] >= lo_key) << e;
+  }
+  gt_m &= valid_m;
+  eq_m &= valid_m & ~gt_m;
+  if (eq_m) {
+#pragma unroll
+    for (int e = 0; e < KPT; ++e)
+      if ((eq_m >> e) & 1u) atomicAdd(&hist2[(key[e] >> 10) & 2047u], 1u);
+  }
+  cluster_sync();  // every CTA's digit-1 reads are done; digit-2 counts are complete
+  cluster_sum(hist2, 2048);
+  find_bin<2048>(gsum, need, wsum, res);
+  const uint32_t d2 = (uint32_t)res[0];
+  need -= (uint32_t)res[1];
+  const uint32_t prefix = (d1 << 11) | d2;
+  const bool whole = gsum[d2] == need;  // the same in every CTA
+  uint32_t T = prefix << 10;
+  if (!whole) {
+    // pass 3: digit 3 of the keys sharing the prefix
+    for (int i = tid; i < 1024; i += kThreads) hist[i] = 0;
+    __syncthreads();
+    if (eq_m) {
+#pragma unroll
+      for (int e = 0; e < KPT; ++e)
+        if (((eq_m >> e) & 1u) && (key[e] >> 10) == prefix) atomicAdd(&hist[key[e] & 1023u], 1u);
+    }
+    cluster_sync();
+    cluster_sum(hist, 1024);
+    find_bin<1024>(gsum, need, wsum, res);
+    T |= (uint32_t)res[0];
+    need -= (uint32_t)res[1];
+  } else {
+    need = 0;
+  }
+  uint32_t sel_m = gt_m, tie_m = 0;
+  if (eq_m) {
+    const uint32_t cut = whole ? T : T + 1u;
+#pragma unroll
+    for (int e = 0; e < KPT; ++e) {
+      const bool in = (eq_m >> e) & 1u;
+      sel_m |= (uint32_t)(in && key[e] >= cut) << e;
+      tie_m |= (uint32_t)(in && !whole && key[e] == T) << e;
+    }
+  }
+  // this CTA's counts in index order, then the CTAs before it in the cluster
+  uint32_t total;
+  const uint32_t excl = block_excl_scan(((uint32_t)__popc(tie_m) << 16) | (uint32_t)__popc(sel_m), wsum, &total);
+  if (tid == 0) cnt[0] = total;
+  cluster_sync();
+  uint32_t before = 0;  // packed (ties << 16 | selected) of the lower-ranked CTAs
+  for (uint32_t k = 0; k < crank; ++k) before += ld_peer(peer_addr(cnt, k));
+  const uint32_t e_before = (before >> 16) + (excl >> 16), s_before = (before & 0xffffu) + (excl & 0xffffu);
+  uint32_t take = need > e_before ? min(need - e_before, (uint32_t)__popc(tie_m)) : 0u;
+  uint32_t rest = tie_m;
+  for (; take > 0; --take) rest &= rest - 1u;
+  uint32_t pick = sel_m | (tie_m ^ rest);
+  uint32_t slot = s_before + min(e_before, need);
+  while (pick) {
+    const int e = __ffs(pick) - 1;
+    if (slot < (uint32_t)kTopK) {  // exactly kTopK; the bound is a guard
+      const int b = v0 + e;
+      ob[slot] = b;
+      const int pos = kBlock * b;
+      const int base = orow ? row_of(ro, pt, r, pos, err, j) : 0;  // a block never straddles a page
+#pragma unroll
+      for (int k = 0; k < kBlock; ++k) {
+        op[kBlock * slot + k] = pos + k;
+        if (orow) orow[kBlock * slot + k] = base < 0 ? -1 : base + k;
+      }
+    }
+    ++slot;
+    pick &= pick - 1u;
+  }
+  if (crank == 0 && tid < kBlock - 1) {
+    const int pos = tid < npart ? kBlock * n + tid : -1;
+    op[kBlock * kTopK + tid] = pos;
+    if (orow) orow[kBlock * kTopK + tid] = pos < 0 ? -1 : row_of(ro, pt, r, pos, err, j);
+  }
+  cluster_sync();  // no CTA leaves while another may still read its counts
+}
+
+template <int KPT>
+cudaError_t launch_topk_cluster(int C, int rows, const float* scores, const int32_t* q_pos, int32_t* sel_blk,
+                                int32_t* sel_pos, int32_t* err, const RowOut& ro, int n_q, int max_blocks,
+                                cudaStream_t s, bool pdl) {
+  const size_t smem = (size_t)kClHdrWords * sizeof(uint32_t);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(rows * C);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<KPT>, scores, q_pos, sel_blk, sel_pos, err, ro, n_q,
+                            max_blocks);
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q_pos,
@@ -454,6 +686,33 @@ cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q
   while ((1 << shift) < d.page_size) ++shift;
   ro.page_shift = shift;
   ro.n_kv = d.n_kv_heads;
+  // Long rows (beyond the register path) and few of them: a cluster of C
+  // CTAs per row, the largest C with every CTA on its own SM, when each CTA's
+  // share of the longest row fits KPT <= 32 keys per thread. (Measured: for
+  // rows the register path holds, the cluster's extra barriers and reductions
+  // cost more than splitting the row saves; a batch-1 262,144-token row takes
+  // the step from 121.6 us to 51.3 us.)
+  const int sms = device_sm_count();
+  int C = 1;
+  for (int c = kMaxCluster; c >= 2; c >>= 1)
+    if ((long long)rows * c <= sms) {
+      C = c;
+      break;
+    }
+  if (C > 1 && mb > kFastCap) {
+    const int per_thread = ((mb + C - 1) / C + kThreads - 1) / kThreads;
+    cudaError_t e = cudaErrorNotSupported;
+    if (per_thread <= 4)
+      e = launch_topk_cluster<4>(C, rows, scores, q_pos, sel_blk, sel_pos, err, ro, d.n_q, mb, s, pdl);
+    else if (per_thread <= 8)
+      e = launch_topk_cluster<8>(C, rows, scores, q_pos, sel_blk, sel_pos, err, ro, d.n_q, mb, s, pdl);
+    else if (per_thread <= 16)
+      e = launch_topk_cluster<16>(C, rows, scores, q_pos, sel_blk, sel_pos, err, ro, d.n_q, mb, s, pdl);
+    else if (per_thread <= 32)
+      e = launch_topk_cluster<32>(C, rows, scores, q_pos, sel_blk, sel_pos, err, ro, d.n_q, mb, s, pdl);
+    if (e == cudaSuccess) return e;
+    cudaGetLastError();  // a cluster the device cannot place: one CTA per row below
+  }
   return launch_k(topk_kernel, dim3(grid), dim3(kThreads), smem, s, pdl, scores, q_pos, sel_blk,
                   sel_pos, err, ro, rows, d.n_q, d.max_blocks, fast_cap, key_cap,
                   (reinterpret_cast<uintptr_t>(scores) & 15u) == 0);

@@ -172,31 +172,38 @@ TOPK_CASES = [
     ("all_equal", 2000), ("all_equal", 65537), ("two_values", 9000), ("ascending", 5000),
     ("descending", 5000), ("signed_zeros", 4000), ("exact_512_top", 7000),
     ("ties_at_threshold", 6000), ("few_bits", 3000), ("few_bits", 60000), ("with_nan", 3000),
+    # longer than the register path: the cluster path at 4 rows
+    ("normal", 32769), ("ties_at_threshold", 40000), ("two_values", 30000), ("with_nan", 26000),
+    ("exact_512_top", 131073),
 ]
 
 
+@pytest.mark.parametrize("batch", [2, 80])
 @pytest.mark.parametrize("kind,n", TOPK_CASES)
-def test_topk_bit_exact_on_shared_scores(qsa, kind, n):
-    # 2 requests x 2 queries: rows of n and a shorter ragged row per request
+def test_topk_bit_exact_on_shared_scores(qsa, kind, n, batch):
+    # requests of 2 queries: rows of n and shorter ragged rows. 160 rows take
+    # one CTA per row; 4 rows longer than the register path take the cluster
+    # path (several CTAs per row).
     n_q = 2
     mb = max(n, 1)
-    lens = [[n, max(0, n - 37)], [max(0, n // 3), n]]
+    lens = ([[n, max(0, n - 37)], [max(0, n // 3), n]] * (batch // 2))[:batch]
     # query k of a row with L full blocks sits at 4L + k - 1 (k partial tokens)
     q_pos = [[max(0, 4 * L + k - 1) for k, L in enumerate(row)] for row in lens]
     for row in q_pos:
         for p in row:
             assert O.n_full(p) <= mb
-    scores = np.stack([np.stack([_score_rows(kind, mb, 100 * r + j) for j in range(n_q)]) for r in range(2)])
-    d = qsa.make_dims(2, n_q, mb, 1, 1)
+    scores = np.stack([np.stack([_score_rows(kind, mb, 100 * (r % 2) + j + 7 * (r // 2)) for j in range(n_q)])
+                       for r in range(batch)])
+    d = qsa.make_dims(batch, n_q, mb, 1, 1)
     ws = qsa.make_workspace(d)
     sc = torch.from_numpy(scores).cuda()
     qp = torch.tensor(q_pos, dtype=torch.int32, device="cuda")
-    sb = torch.full((2, n_q, 512), 7, dtype=torch.int32, device="cuda")
-    sp = torch.full((2, n_q, 2051), 7, dtype=torch.int32, device="cuda")
+    sb = torch.full((batch, n_q, 512), 7, dtype=torch.int32, device="cuda")
+    sp = torch.full((batch, n_q, 2051), 7, dtype=torch.int32, device="cuda")
     qsa.topk(d, sc, qp, sb, sp, ws)
     _check_ok(qsa, ws)
     gb, gp = sb.cpu().numpy(), sp.cpu().numpy()
-    for r in range(2):
+    for r in (range(batch) if batch <= 2 else (0, 1, 2, 3, batch // 2, batch - 2, batch - 1)):
         for j in range(n_q):
             p = q_pos[r][j]
             ref_b = O.topk_blocks(scores[r, j, : O.n_full(p)])
