@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--no-flush", action="store_true", help="warm-L2 numbers (reported as such)")
     ap.add_argument("--step-only", action="store_true",
                     help="only the warm-up and timed fused steps (for profiler captures)")
+    ap.add_argument("--paged-kc", action="store_true",
+                    help="the compressed keys in the KV cache's pages (qsa_decode_paged)")
     ap.add_argument("--draft", action="store_true",
                     help="time an MTP draft step instead: one draft query per request attending over the "
                          "selection of the request's first verify query plus the 3 positions after it")
@@ -213,8 +215,9 @@ def make_gpu_state(qsa, spec):
 
 def decode_call(qsa, st, inputs=None, out=None):
     g = st["g"] if inputs is None else inputs
-    qsa.decode(st["d"], g["q_idx"], st["kc"], g["q"], st["g"]["k_cache"], st["g"]["v_cache"], st["g"]["k_scale"],
-               st["g"]["v_scale"], g["page_table"], g["q_pos"], st["out"] if out is None else out, st["ws"])
+    fn = qsa.decode_paged if st.get("paged_kc") else qsa.decode
+    fn(st["d"], g["q_idx"], st["kc"], g["q"], st["g"]["k_cache"], st["g"]["v_cache"], st["g"]["k_scale"],
+       st["g"]["v_scale"], g["page_table"], g["q_pos"], st["out"] if out is None else out, st["ws"])
 
 
 def timed(fn, steps, flush, stream):
@@ -355,15 +358,25 @@ def run_ours(args, world, rank):
     qsa = build_lib()
     spec = synth.spec_for(args.config, batch=args.batch, ctx=args.ctx)
     st = make_gpu_state(qsa, spec)
+    if args.paged_kc:
+        g = st["g"]
+        kcp = torch.zeros((spec.num_pages(), spec.page_size // 4, spec.n_idx_heads, spec.head_dim),
+                          dtype=torch.bfloat16, device="cuda")
+        idx_keys = synth.normal_bf16((spec.batch, 4 * spec.max_blocks(), spec.n_idx_heads, spec.head_dim),
+                                     spec.seed + synth.T_IDXKEYS, device="cuda")
+        qsa.compress_keys_paged(st["d"], idx_keys, g["q_pos"], g["page_table"], kcp, st["ws"])
+        del idx_keys
+        st["kc"], st["paged_kc"] = kcp, True
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     flush = None if args.no_flush else torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
 
     # one checked step: its selection gives the byte count
     d = st["d"]
-    qsa.decode(d, st["g"]["q_idx"], st["kc"], st["g"]["q"], st["g"]["k_cache"], st["g"]["v_cache"],
-               st["g"]["k_scale"], st["g"]["v_scale"], st["g"]["page_table"], st["g"]["q_pos"], st["out"],
-               st["ws"], scores=st["scores"], sel_blk=st["sel_blk"], sel_pos=st["sel_pos"])
+    (qsa.decode_paged if args.paged_kc else qsa.decode)(
+        d, st["g"]["q_idx"], st["kc"], st["g"]["q"], st["g"]["k_cache"], st["g"]["v_cache"], st["g"]["k_scale"],
+        st["g"]["v_scale"], st["g"]["page_table"], st["g"]["q_pos"], st["out"], st["ws"], scores=st["scores"],
+        sel_blk=st["sel_blk"], sel_pos=st["sel_pos"])
     status, info = qsa.check_errors(st["ws"])
     if status != qsa.OK:
         raise RuntimeError(f"device error during the step: {info}")
@@ -407,8 +420,10 @@ def run_ours(args, world, rank):
     g = st["g"]
     reps = max(20, min(args.steps, 200))
     k_ms = {
-        "score": statistics.mean(timed(lambda: qsa.score(d, g["q_idx"], st["kc"], g["q_pos"], st["scores"], st["ws"]),
-                                       reps, flush, stream)),
+        "score": statistics.mean(timed(
+            (lambda: qsa.score_paged(d, g["q_idx"], st["kc"], g["page_table"], g["q_pos"], st["scores"], st["ws"]))
+            if args.paged_kc else (lambda: qsa.score(d, g["q_idx"], st["kc"], g["q_pos"], st["scores"], st["ws"])),
+            reps, flush, stream)),
         "topk": statistics.mean(timed(lambda: qsa.topk(d, st["scores"], g["q_pos"], st["sel_blk"], st["sel_pos"],
                                                        st["ws"]), reps, flush, stream)),
         "sparse_attn": statistics.mean(timed(lambda: qsa.sparse_attn(d, g["q"], g["k_cache"], g["v_cache"],
@@ -490,6 +505,7 @@ def run_ours(args, world, rank):
             "config": {"workload": spec.name, "batch": spec.batch, "n_q": spec.n_q,
                        "contexts": "50000+800*t, t~U{0..14}" if args.config in (2, 3) else str(spec.first_pos[0]),
                        "n_idx_heads": spec.n_idx_heads, "kv": spec.kv_dtype, "page_size": spec.page_size,
+                       "compressed_keys": "in the KV pages" if args.paged_kc else "contiguous per request",
                        "l2": "no flush (warm)" if flush is None else "flushed before every step (write of 2x L2)",
                        "parallelism": f"replicas x{world}"},
             "bytes_per_step": {"kc": int(b_kc), "kv_union": int(b_kv_union), "kv_sum": int(b_kv_sum)},

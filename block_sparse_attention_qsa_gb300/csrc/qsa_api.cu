@@ -158,6 +158,32 @@ qsa_status qsa_compress_keys(const qsa_dims* dims, const void* idx_keys, const i
   return from_cuda(e);
 }
 
+qsa_status qsa_compress_keys_paged(const qsa_dims* dims, const void* idx_keys, const int32_t* q_pos,
+                                   const int32_t* block_lo, const int32_t* page_table, void* kc_cache,
+                                   void* ws, size_t ws_bytes, void* stream) {
+  qsa_status st = check_dims(dims);
+  if (st != QSA_OK) return st;
+  if (!idx_keys || !q_pos || !page_table || !kc_cache) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(idx_keys) || !aligned16(kc_cache)) return QSA_ERR_INVALID_ARG;
+  if ((st = check_ws(dims, ws, ws_bytes, nullptr)) != QSA_OK) return st;
+  return from_cuda(launch_compress(*dims, static_cast<const __nv_bfloat16*>(idx_keys), q_pos, block_lo,
+                                   static_cast<__nv_bfloat16*>(kc_cache), err_word(ws),
+                                   static_cast<cudaStream_t>(stream), page_table));
+}
+
+qsa_status qsa_score_paged(const qsa_dims* dims, const void* q_idx, const void* kc_cache,
+                           const int32_t* page_table, const int32_t* q_pos, float* scores, void* ws,
+                           size_t ws_bytes, void* stream) {
+  qsa_status st = check_dims(dims);
+  if (st != QSA_OK) return st;
+  if (!q_idx || !kc_cache || !page_table || !q_pos || !scores) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(kc_cache)) return QSA_ERR_INVALID_ARG;
+  if ((st = check_ws(dims, ws, ws_bytes, nullptr)) != QSA_OK) return st;
+  return from_cuda(launch_score(*dims, static_cast<const __nv_bfloat16*>(q_idx),
+                                static_cast<const __nv_bfloat16*>(kc_cache), q_pos, scores, err_word(ws),
+                                static_cast<cudaStream_t>(stream), false, page_table));
+}
+
 qsa_status qsa_score(const qsa_dims* dims, const void* q_idx, const void* kc, const int32_t* q_pos,
                      float* scores, void* ws, size_t ws_bytes, void* stream) {
   qsa_status st = check_dims(dims);
@@ -202,11 +228,15 @@ qsa_status qsa_sparse_attn(const qsa_dims* dims, const void* q, const void* k_ca
                                at<int32_t>(ws, w.tickets), at<float>(ws, w.partials), pl, s, true));
 }
 
-qsa_status qsa_decode(const qsa_dims* dims, const void* q_idx, const void* kc, const void* q,
-                      const void* k_cache, const void* v_cache, const float* k_scale,
-                      const float* v_scale, const int32_t* page_table, const int32_t* q_pos,
-                      float* scores, int32_t* sel_blk, int32_t* sel_pos, void* out, void* ws,
-                      size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The fused step; kc_paged: the compressed keys live in the KV cache's pages.
+qsa_status decode_impl(const qsa_dims* dims, const void* q_idx, const void* kc, const void* q,
+                       const void* k_cache, const void* v_cache, const float* k_scale, const float* v_scale,
+                       const int32_t* page_table, const int32_t* q_pos, float* scores, int32_t* sel_blk,
+                       int32_t* sel_pos, void* out, void* ws, size_t ws_bytes, void* stream, bool kc_paged) {
   qsa_status st = check_dims(dims);
   if (st != QSA_OK) return st;
   if (!q_idx || !kc || !q || !k_cache || !v_cache || !page_table || !q_pos || !out)
@@ -222,7 +252,8 @@ qsa_status qsa_decode(const qsa_dims* dims, const void* q_idx, const void* kc, c
   int32_t* sb = sel_blk ? sel_blk : at<int32_t>(ws, w.sel_blk);
   int32_t* spos = sel_pos ? sel_pos : at<int32_t>(ws, w.sel_pos);
   cudaError_t e = launch_score(*dims, static_cast<const __nv_bfloat16*>(q_idx),
-                               static_cast<const __nv_bfloat16*>(kc), q_pos, sc, err_word(ws), s, false);
+                               static_cast<const __nv_bfloat16*>(kc), q_pos, sc, err_word(ws), s, false,
+                               kc_paged ? page_table : nullptr);
   if (e != cudaSuccess) return QSA_ERR_CUDA;
   int32_t* srow = at<int32_t>(ws, w.sel_row);
   e = launch_topk(*dims, sc, q_pos, sb, spos, err_word(ws), page_table, srow, s, true);
@@ -231,6 +262,28 @@ qsa_status qsa_decode(const qsa_dims* dims, const void* q_idx, const void* kc, c
   e = launch_attn(*dims, q, k_cache, v_cache, k_scale, v_scale, srow, out, at<int32_t>(ws, w.tickets),
                   at<float>(ws, w.partials), pl, s, true);
   return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+qsa_status qsa_decode(const qsa_dims* dims, const void* q_idx, const void* kc, const void* q,
+                      const void* k_cache, const void* v_cache, const float* k_scale,
+                      const float* v_scale, const int32_t* page_table, const int32_t* q_pos,
+                      float* scores, int32_t* sel_blk, int32_t* sel_pos, void* out, void* ws,
+                      size_t ws_bytes, void* stream) {
+  return decode_impl(dims, q_idx, kc, q, k_cache, v_cache, k_scale, v_scale, page_table, q_pos, scores, sel_blk,
+                     sel_pos, out, ws, ws_bytes, stream, false);
+}
+
+qsa_status qsa_decode_paged(const qsa_dims* dims, const void* q_idx, const void* kc_cache, const void* q,
+                            const void* k_cache, const void* v_cache, const float* k_scale,
+                            const float* v_scale, const int32_t* page_table, const int32_t* q_pos,
+                            float* scores, int32_t* sel_blk, int32_t* sel_pos, void* out, void* ws,
+                            size_t ws_bytes, void* stream) {
+  return decode_impl(dims, q_idx, kc_cache, q, k_cache, v_cache, k_scale, v_scale, page_table, q_pos, scores,
+                     sel_blk, sel_pos, out, ws, ws_bytes, stream, true);
 }
 
 qsa_status qsa_draft_attn(const qsa_dims* dims, const void* q, const void* k_cache, const void* v_cache,

@@ -109,14 +109,24 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// Where the compressed keys live: contiguous [B][max_blocks][H][128] (table
+// null) or in the KV cache's pages, [num_pages][page_size / 4][H][128], found
+// through the request's page table (block b of request r: page
+// table[r][b >> bpp_shift], slot b & ((1 << bpp_shift) - 1)).
+struct KcPages {
+  const int32_t* table;  // [B][max_pages], or null: contiguous
+  int max_pages, num_pages, bpp_shift;
+};
+
 // ---------------------------------------------------------------------------
 // launchers implemented in the kernel translation units
 // ---------------------------------------------------------------------------
 cudaError_t launch_compress(const qsa_dims& d, const __nv_bfloat16* idx_keys, const int32_t* q_pos,
                             const int32_t* block_lo, __nv_bfloat16* kc, int32_t* err,
-                            cudaStream_t s);
+                            cudaStream_t s, const int32_t* page_table = nullptr);
 cudaError_t launch_score(const qsa_dims& d, const __nv_bfloat16* q_idx, const __nv_bfloat16* kc,
-                         const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s, bool pdl);
+                         const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s, bool pdl,
+                         const int32_t* page_table = nullptr);
 // page_table / sel_row (optional, inside qsa_decode): also write each selected
 // position's cache row for KV head 0, so attention skips the page lookup
 cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q_pos,

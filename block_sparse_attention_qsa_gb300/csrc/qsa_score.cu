@@ -34,11 +34,25 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 // ---------------------------------------------------------------------------
 // compressed keys: kc[r][b] = bf16( (((k0 + k1) + k2) + k3) * 0.25 ), FP32
 // ---------------------------------------------------------------------------
+// the 16-byte chunks of block b's compressed key row of request r, or null
+// for a page outside the cache (recorded)
+__device__ __forceinline__ uint4* kc_row(uint4* kc, const KcPages& kp, int r, int b, int max_blocks, int cpb,
+                                         int32_t* err) {
+  if (!kp.table) return kc + ((size_t)r * max_blocks + b) * cpb;
+  const int pi = b >> kp.bpp_shift;
+  const int page = pi < kp.max_pages ? kp.table[(size_t)r * kp.max_pages + pi] : -1;
+  if (page < 0 || page >= kp.num_pages) {
+    record_error(err, kErrPage, r, 0, page);
+    return nullptr;
+  }
+  return kc + ((((size_t)page) << kp.bpp_shift) + (b & ((1 << kp.bpp_shift) - 1))) * cpb;
+}
+
 __global__ void __launch_bounds__(256) compress_kernel(const uint4* __restrict__ idx_keys,
                                                        const int32_t* __restrict__ q_pos,
                                                        const int32_t* __restrict__ block_lo,
                                                        uint4* __restrict__ kc, int32_t* err,
-                                                       int n_q, int H, int max_blocks) {
+                                                       int n_q, int H, int max_blocks, const KcPages kp) {
   const int r = blockIdx.y;
   __shared__ int s_lo, s_hi;
   if (threadIdx.x == 0) {
@@ -58,7 +72,6 @@ __global__ void __launch_bounds__(256) compress_kernel(const uint4* __restrict__
   const int cpb = H * 16;  // 16-byte chunks per token row
   const long long total = (long long)max(0, s_hi - s_lo) * cpb;
   const uint4* src_r = idx_keys + (size_t)r * max_blocks * kBlock * cpb;
-  uint4* dst_r = kc + (size_t)r * max_blocks * cpb;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
     const int b = s_lo + (int)(i / cpb);
@@ -80,7 +93,8 @@ __global__ void __launch_bounds__(256) compress_kernel(const uint4* __restrict__
       const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
       ow[w] = *reinterpret_cast<const uint32_t*>(&h);
     }
-    dst_r[(size_t)b * cpb + c] = o;
+    uint4* dst = kc_row(kc, kp, r, b, max_blocks, cpb, err);
+    if (dst) dst[c] = o;
   }
 }
 
@@ -124,12 +138,12 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int H>
+template <int H, bool PAGED>
 __global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(const __nv_bfloat16* __restrict__ q_idx,
                                                     const uint4* __restrict__ kc,
                                                     const int32_t* __restrict__ q_pos,
                                                     float* __restrict__ scores, int32_t* err,
-                                                    int B, int n_q, int max_blocks) {
+                                                    int B, int n_q, int max_blocks, const KcPages kp) {
   using Geo = ScoreGeom<H>;
   constexpr int STEPS = Geo::STEPS, PD = Geo::PD;
   constexpr int CPB = H * 16;  // 16-B chunks per block row
@@ -219,19 +233,57 @@ __global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(cons
     const uint4* kc_r = kc + (size_t)r * max_blocks * CPB;
     float* sc_r = scores + (size_t)r * n_q * max_blocks;
 
+    // paged keys: the page ids of a batch's rows g and g + 8 are loaded one
+    // batch ahead, so the key loads do not wait for the page table
+    const int32_t* pt_r = PAGED ? kp.table + (size_t)r * kp.max_pages : nullptr;
+    int pg[PD][2];
+    auto load_pages = [&](int ub) {
+#pragma unroll
+      for (int k = 0; k < PD; ++k) {
+        const int b = (ub + k - u0) * 16 + g;
+        const bool in = ub + k < seg_end;
+        // a page index past the table reads as page -1 (reported as a bad page)
+        const int i0 = b >> kp.bpp_shift, i1 = (b + 8) >> kp.bpp_shift;
+        pg[k][0] = (in && b < nb_r) ? (i0 < kp.max_pages ? pt_r[i0] : -1) : -1;
+        pg[k][1] = (in && b + 8 < nb_r) ? (i1 < kp.max_pages ? pt_r[i1] : -1) : -1;
+      }
+    };
+    if constexpr (PAGED) load_pages(u);
     for (; u < seg_end; u += PD) {
       uint4 lo_v[PD][STEPS], hi_v[PD][STEPS];
+      int pc[PD][2];
+      if constexpr (PAGED) {
+#pragma unroll
+        for (int k = 0; k < PD; ++k) {
+          pc[k][0] = pg[k][0];
+          pc[k][1] = pg[k][1];
+        }
+        if (u + PD < seg_end) load_pages(u + PD);
+      }
 #pragma unroll
       for (int k = 0; k < PD; ++k) {
         const int b = (u + k - u0) * 16 + g;
         const bool in = u + k < seg_end;
         const bool ok0 = in && b < nb_r, ok1 = in && b + 8 < nb_r;
-        const uint4* row0 = kc_r + (size_t)b * CPB + c;
-        const uint4* row1 = row0 + (size_t)8 * CPB;
+        const uint4* row0;
+        const uint4* row1;
+        bool okp0 = ok0, okp1 = ok1;
+        if constexpr (PAGED) {
+          const int bm = (1 << kp.bpp_shift) - 1;
+          okp0 = ok0 && pc[k][0] >= 0 && pc[k][0] < kp.num_pages;
+          okp1 = ok1 && pc[k][1] >= 0 && pc[k][1] < kp.num_pages;
+          if (ok0 && !okp0) record_error(err, kErrPage, r, 0, pc[k][0]);
+          if (ok1 && !okp1) record_error(err, kErrPage, r, 0, pc[k][1]);
+          row0 = kc + (okp0 ? ((((size_t)pc[k][0]) << kp.bpp_shift) + (b & bm)) * CPB : 0) + c;
+          row1 = kc + (okp1 ? ((((size_t)pc[k][1]) << kp.bpp_shift) + ((b + 8) & bm)) * CPB : 0) + c;
+        } else {
+          row0 = kc_r + (size_t)b * CPB + c;
+          row1 = row0 + (size_t)8 * CPB;
+        }
 #pragma unroll
         for (int s = 0; s < STEPS; ++s) {
-          lo_v[k][s] = ok0 ? ld_stream(row0 + 4 * s) : make_uint4(0, 0, 0, 0);
-          hi_v[k][s] = ok1 ? ld_stream(row1 + 4 * s) : make_uint4(0, 0, 0, 0);
+          lo_v[k][s] = okp0 ? ld_stream(row0 + 4 * s) : make_uint4(0, 0, 0, 0);
+          hi_v[k][s] = okp1 ? ld_stream(row1 + 4 * s) : make_uint4(0, 0, 0, 0);
         }
       }
 #pragma unroll
@@ -257,13 +309,28 @@ __global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(cons
   }
 }
 
-template <int H>
+int shift_of(int x) {
+  int sh = 0;
+  while ((1 << sh) < x) ++sh;
+  return sh;
+}
+
+KcPages kc_pages(const qsa_dims& d, const int32_t* page_table) {
+  KcPages kp;
+  kp.table = page_table;
+  kp.max_pages = d.max_pages;
+  kp.num_pages = d.num_pages;
+  kp.bpp_shift = shift_of(d.page_size / kBlock);
+  return kp;
+}
+
+template <int H, bool PAGED>
 cudaError_t launch_score_h(const qsa_dims& d, const __nv_bfloat16* q_idx, const __nv_bfloat16* kc,
                            const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s,
-                           bool pdl) {
-  auto kern = score_kernel<H>;
+                           bool pdl, const KcPages& kp) {
+  auto kern = score_kernel<H, PAGED>;
   const size_t smem = (size_t)(2 * d.batch + 1) * sizeof(int);
-  static int occ_cache[64] = {0};
+  static int occ_cache[64] = {0};  // one per instantiation
   int dev = 0;
   cudaGetDevice(&dev);
   int occ = dev < 64 ? occ_cache[dev] : 0;
@@ -280,14 +347,14 @@ cudaError_t launch_score_h(const qsa_dims& d, const __nv_bfloat16* q_idx, const 
   if (want < warps) warps = want;
   const int grid = (int)((warps + 7) / 8 > 0 ? (warps + 7) / 8 : 1);
   return launch_k(kern, dim3(grid), dim3(256), smem, s, pdl, q_idx, reinterpret_cast<const uint4*>(kc), q_pos,
-                  scores, err, d.batch, d.n_q, d.max_blocks);
+                  scores, err, d.batch, d.n_q, d.max_blocks, kp);
 }
 
 }  // namespace
 
 cudaError_t launch_compress(const qsa_dims& d, const __nv_bfloat16* idx_keys, const int32_t* q_pos,
                             const int32_t* block_lo, __nv_bfloat16* kc, int32_t* err,
-                            cudaStream_t s) {
+                            cudaStream_t s, const int32_t* page_table) {
   const long long chunks = (long long)d.max_blocks * d.n_idx_heads * 16;
   long long gx = (chunks + 255) / 256;
   const long long cap = (long long)device_sm_count() * 8;
@@ -295,17 +362,26 @@ cudaError_t launch_compress(const qsa_dims& d, const __nv_bfloat16* idx_keys, co
   if (gx < 1) gx = 1;
   return launch_k(compress_kernel, dim3((unsigned)gx, d.batch), dim3(256), 0, s, false,
                   reinterpret_cast<const uint4*>(idx_keys), q_pos, block_lo,
-                  reinterpret_cast<uint4*>(kc), err, d.n_q, d.n_idx_heads, d.max_blocks);
+                  reinterpret_cast<uint4*>(kc), err, d.n_q, d.n_idx_heads, d.max_blocks, kc_pages(d, page_table));
 }
 
 cudaError_t launch_score(const qsa_dims& d, const __nv_bfloat16* q_idx, const __nv_bfloat16* kc,
                          const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s,
-                         bool pdl) {
+                         bool pdl, const int32_t* page_table) {
+  const KcPages kp = kc_pages(d, page_table);
+  if (page_table) {
+    switch (d.n_idx_heads) {
+      case 1: return launch_score_h<1, true>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp);
+      case 2: return launch_score_h<2, true>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp);
+      case 3: return launch_score_h<3, true>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp);
+      default: return launch_score_h<4, true>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp);
+    }
+  }
   switch (d.n_idx_heads) {
-    case 1: return launch_score_h<1>(d, q_idx, kc, q_pos, scores, err, s, pdl);
-    case 2: return launch_score_h<2>(d, q_idx, kc, q_pos, scores, err, s, pdl);
-    case 3: return launch_score_h<3>(d, q_idx, kc, q_pos, scores, err, s, pdl);
-    default: return launch_score_h<4>(d, q_idx, kc, q_pos, scores, err, s, pdl);
+    case 1: return launch_score_h<1, false>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp);
+    case 2: return launch_score_h<2, false>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp);
+    case 3: return launch_score_h<3, false>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp);
+    default: return launch_score_h<4, false>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp);
   }
 }
 

@@ -32,6 +32,7 @@ EXPORTS = (
     "qsa_abi_version", "qsa_status_str", "qsa_dims_default", "qsa_workspace_size",
     "qsa_workspace_init", "qsa_compress_keys", "qsa_score", "qsa_topk", "qsa_sparse_attn",
     "qsa_decode", "qsa_check_errors", "qsa_sparse_attn_noalloc", "qsa_draft_attn",
+    "qsa_compress_keys_paged", "qsa_score_paged", "qsa_decode_paged",
 )
 
 MAX_DRAFT_GAP = 64  # QSA_MAX_DRAFT_GAP
@@ -77,6 +78,9 @@ def _load() -> ctypes.CDLL:
         "qsa_check_errors": (I, [P, P, ctypes.POINTER(ctypes.c_int32)]),
         "qsa_sparse_attn_noalloc": (I, [D, P, P, P, P, P, P, P, P, P, P]),
         "qsa_draft_attn": (I, [D, P, P, P, P, P, P, P, P, ctypes.c_int32, P, P, P, P, SZ, P]),
+        "qsa_compress_keys_paged": (I, [D, P, P, P, P, P, P, SZ, P]),
+        "qsa_score_paged": (I, [D, P, P, P, P, P, P, SZ, P]),
+        "qsa_decode_paged": (I, [D, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -233,6 +237,54 @@ def sparse_attn_noalloc(d: Dims, q, k_cache, v_cache, k_scale, v_scale, page_tab
     _check(lib.qsa_sparse_attn_noalloc(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                        _ptr(v_scale), _ptr(page_table), _ptr(sel_pos), _ptr(q_pos), _ptr(out),
                                        _stream(stream)), "qsa_sparse_attn_noalloc")
+
+
+def _want_kc_cache(d: Dims, kc_cache):
+    _want(kc_cache, "kc_cache", (d.num_pages, d.page_size // d.block, d.n_idx_heads, d.idx_dim), torch.bfloat16)
+
+
+def compress_keys_paged(d: Dims, idx_keys, q_pos, page_table, kc_cache, ws, block_lo=None, stream=None):
+    """compress_keys into the paged layout [num_pages][page_size / 4][H_idx][128]."""
+    _want(idx_keys, "idx_keys", (d.batch, d.block * d.max_blocks, d.n_idx_heads, d.idx_dim), torch.bfloat16)
+    _want(q_pos, "q_pos", (d.batch, d.n_q), torch.int32)
+    _want(page_table, "page_table", (d.batch, d.max_pages), torch.int32)
+    _want_kc_cache(d, kc_cache)
+    if block_lo is not None:
+        _want(block_lo, "block_lo", (d.batch,), torch.int32)
+    w, n = _ws(d, ws)
+    _check(lib.qsa_compress_keys_paged(ctypes.byref(d), _ptr(idx_keys), _ptr(q_pos), _ptr(block_lo),
+                                       _ptr(page_table), _ptr(kc_cache), w, n, _stream(stream)),
+           "qsa_compress_keys_paged")
+
+
+def score_paged(d: Dims, q_idx, kc_cache, page_table, q_pos, scores, ws, stream=None):
+    _want(q_idx, "q_idx", (d.batch, d.n_q, d.n_idx_heads, d.idx_dim), torch.bfloat16)
+    _want_kc_cache(d, kc_cache)
+    _want(page_table, "page_table", (d.batch, d.max_pages), torch.int32)
+    _want(q_pos, "q_pos", (d.batch, d.n_q), torch.int32)
+    _want(scores, "scores", (d.batch, d.n_q, d.max_blocks), torch.float32)
+    w, n = _ws(d, ws)
+    _check(lib.qsa_score_paged(ctypes.byref(d), _ptr(q_idx), _ptr(kc_cache), _ptr(page_table), _ptr(q_pos),
+                               _ptr(scores), w, n, _stream(stream)), "qsa_score_paged")
+
+
+def decode_paged(d: Dims, q_idx, kc_cache, q, k_cache, v_cache, k_scale, v_scale, page_table, q_pos, out, ws,
+                 scores=None, sel_blk=None, sel_pos=None, stream=None):
+    """decode with the compressed keys in the KV cache's pages."""
+    _want(q_idx, "q_idx", (d.batch, d.n_q, d.n_idx_heads, d.idx_dim), torch.bfloat16)
+    _want_kc_cache(d, kc_cache)
+    _check_attn_inputs(d, q, k_cache, v_cache, k_scale, v_scale, page_table, q_pos, out)
+    if scores is not None:
+        _want(scores, "scores", (d.batch, d.n_q, d.max_blocks), torch.float32)
+    if sel_blk is not None:
+        _want(sel_blk, "sel_blk", (d.batch, d.n_q, d.topk), torch.int32)
+    if sel_pos is not None:
+        _want(sel_pos, "sel_pos", (d.batch, d.n_q, d.width), torch.int32)
+    w, n = _ws(d, ws)
+    _check(lib.qsa_decode_paged(ctypes.byref(d), _ptr(q_idx), _ptr(kc_cache), _ptr(q), _ptr(k_cache),
+                                _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(page_table), _ptr(q_pos),
+                                _ptr(scores), _ptr(sel_blk), _ptr(sel_pos), _ptr(out), w, n, _stream(stream)),
+           "qsa_decode_paged")
 
 
 def draft_attn(d: Dims, q, k_cache, v_cache, k_scale, v_scale, page_table, sel_pos, sel_q_pos, src, q_pos,

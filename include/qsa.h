@@ -211,6 +211,28 @@ qsa_status qsa_sparse_attn_noalloc(const qsa_dims* dims, const void* q, const vo
                                    const int32_t* page_table, const int32_t* sel_pos,
                                    const int32_t* q_pos, void* out, void* stream);
 
+/* Paged compressed keys (the pages place the selected history "in the
+ * cache", 10100.com "第一处"; here the compressed keys live in the KV
+ * cache's pages too, found through the same page table). kc_cache is
+ * [num_pages][page_size / 4][n_idx_heads][128] BF16: page p holds the
+ * compressed keys of the page_size / 4 blocks whose tokens it holds; block b
+ * of request r is slot b % (page_size / 4) of page
+ * page_table[r][b / (page_size / 4)]. Same arithmetic and results, bit for
+ * bit, as qsa_compress_keys / qsa_score / qsa_decode on the contiguous
+ * layout. A page id outside the cache is reported (kind 2) and its blocks are
+ * skipped (not written; scored as zero). */
+qsa_status qsa_compress_keys_paged(const qsa_dims* dims, const void* idx_keys, const int32_t* q_pos,
+                                   const int32_t* block_lo, const int32_t* page_table, void* kc_cache,
+                                   void* ws, size_t ws_bytes, void* stream);
+qsa_status qsa_score_paged(const qsa_dims* dims, const void* q_idx, const void* kc_cache,
+                           const int32_t* page_table, const int32_t* q_pos, float* scores, void* ws,
+                           size_t ws_bytes, void* stream);
+qsa_status qsa_decode_paged(const qsa_dims* dims, const void* q_idx, const void* kc_cache, const void* q,
+                            const void* k_cache, const void* v_cache, const float* k_scale,
+                            const float* v_scale, const int32_t* page_table, const int32_t* q_pos,
+                            float* scores, int32_t* sel_blk, int32_t* sel_pos, void* out, void* ws,
+                            size_t ws_bytes, void* stream);
+
 /* MTP draft steps reusing an earlier selection (arex-research.com, section
  * "四类优化" heading: "MTP 复用"; 10100.com, "第三处": later draft steps reuse
  * the attention positions selected before, instead of scoring and selecting

@@ -401,6 +401,54 @@ def _run_decode(qsa, spec, g):
 
 
 # --------------------------------------------------------------------------
+# compressed keys in the KV cache's pages (qsa_*_paged)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("page_size,h,kv", [(64, 1, "bf16"), (16, 4, "fp8"), (128, 2, "bf16")])
+def test_paged_compressed_keys_match_the_contiguous_path(qsa, page_size, h, kv):
+    spec = synth.Spec(f"paged-kc-{page_size}", 3, 4, [3001, 1498, 5000], h, kv, True, 91 + page_size,
+                      page_size=page_size)
+    inp = synth.make_inputs(spec)
+    g = _dev(inp)
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    B, mb, bpp = spec.batch, spec.max_blocks(), page_size // 4
+    kc = torch.zeros((B, mb, h, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.compress_keys(d, g["idx_keys"], g["q_pos"], kc, ws)
+    kcp = torch.zeros((spec.num_pages(), bpp, h, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.compress_keys_paged(d, g["idx_keys"], g["q_pos"], g["page_table"], kcp, ws)
+    _check_ok(qsa, ws)
+    kc_h, kcp_h, pt = bits(kc), bits(kcp), inp["page_table"].numpy()
+    for r in range(B):
+        nb = O.n_full(max(spec.q_pos()[r]))
+        b = np.arange(nb)
+        assert np.array_equal(kcp_h[pt[r, b // bpp], b % bpp], kc_h[r, :nb]), r
+    # scores: bit for bit
+    sc = torch.full((B, 4, mb), float("nan"), device="cuda")
+    scp = torch.full((B, 4, mb), float("nan"), device="cuda")
+    qsa.score(d, g["q_idx"], kc, g["q_pos"], sc, ws)
+    qsa.score_paged(d, g["q_idx"], kcp, g["page_table"], g["q_pos"], scp, ws)
+    _check_ok(qsa, ws)
+    sc_h, scp_h = sc.cpu().numpy(), scp.cpu().numpy()
+    for r in range(B):
+        for j in range(4):
+            n = O.n_full(spec.q_pos()[r][j])
+            assert np.array_equal(sc_h[r, j, :n].view(np.uint32), scp_h[r, j, :n].view(np.uint32)), (r, j)
+    # the fused step: the same selection and output, bit for bit
+    outs = []
+    for paged in (False, True):
+        out = torch.empty((B, 4, 16, 128), dtype=torch.bfloat16, device="cuda")
+        sp = torch.empty((B, 4, 2051), dtype=torch.int32, device="cuda")
+        fn = qsa.decode_paged if paged else qsa.decode
+        fn(d, g["q_idx"], kcp if paged else kc, g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"],
+           g["page_table"], g["q_pos"], out, ws, sel_pos=sp)
+        _check_ok(qsa, ws)
+        outs.append((bits(out), sp.cpu().numpy()))
+    assert np.array_equal(outs[0][1], outs[1][1])
+    assert np.array_equal(outs[0][0], outs[1][0])
+
+
+# --------------------------------------------------------------------------
 # MTP draft steps reusing an earlier selection (qsa_draft_attn)
 # --------------------------------------------------------------------------
 
