@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--no-flush", action="store_true", help="warm-L2 numbers (reported as such)")
     ap.add_argument("--step-only", action="store_true",
                     help="only the warm-up and timed fused steps (for profiler captures)")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time direct calls instead of replaying the step captured as a CUDA graph")
     ap.add_argument("--paged-kc", action="store_true",
                     help="the compressed keys in the KV cache's pages (qsa_decode_paged)")
     ap.add_argument("--draft", action="store_true",
@@ -387,11 +389,25 @@ def run_ours(args, world, rank):
     if args.draft:
         return run_draft(qsa, args, spec, st, sel_host, flush, stream, world, rank)
 
-    # warm-up, then exactly K timed steps
+    # warm-up, then exactly K timed steps. The step is captured once as a CUDA
+    # graph (its three kernels and their programmatic dependencies), as a
+    # serving loop would run it, and replayed; --no-graph times direct calls.
+    step_fn = lambda: decode_call(qsa, st)
+    if not args.no_graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                decode_call(qsa, st)
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            decode_call(qsa, st)
+        step_fn = graph.replay
     for _ in range(args.warmup):
         if flush is not None:
             flush.zero_()
-        decode_call(qsa, st)
+        step_fn()
     torch.cuda.synchronize()
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
@@ -400,7 +416,7 @@ def run_ours(args, world, rank):
     torch.cuda.synchronize()
     if sampler:
         sampler.mark("start")
-    step_ms = timed(lambda: decode_call(qsa, st), args.steps, flush, stream)
+    step_ms = timed(step_fn, args.steps, flush, stream)
     torch.cuda.synchronize()
     barrier(world)
     if sampler:
@@ -507,6 +523,7 @@ def run_ours(args, world, rank):
                        "n_idx_heads": spec.n_idx_heads, "kv": spec.kv_dtype, "page_size": spec.page_size,
                        "compressed_keys": "in the KV pages" if args.paged_kc else "contiguous per request",
                        "l2": "no flush (warm)" if flush is None else "flushed before every step (write of 2x L2)",
+                       "launch": "direct calls" if args.no_graph else "the step captured once as a CUDA graph, replayed",
                        "parallelism": f"replicas x{world}"},
             "bytes_per_step": {"kc": int(b_kc), "kv_union": int(b_kv_union), "kv_sum": int(b_kv_sum)},
             "kernels": kernels, "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
