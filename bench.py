@@ -60,6 +60,8 @@ def parse_args():
                     help="time direct calls instead of replaying the step captured as a CUDA graph")
     ap.add_argument("--paged-kc", action="store_true",
                     help="the compressed keys in the KV cache's pages (qsa_decode_paged)")
+    ap.add_argument("--chunk", type=int, default=0,
+                    help="time chunked scoring instead: one request (config 1's 50K context), this many queries")
     ap.add_argument("--draft", action="store_true",
                     help="time an MTP draft step instead: one draft query per request attending over the "
                          "selection of the request's first verify query plus the 3 positions after it")
@@ -356,8 +358,51 @@ def run_draft(qsa, args, spec, st, sel_host, flush, stream, world, rank):
                           "note": "entry-point time: positions resolved to cache rows, then attention"}))
 
 
+def run_chunk(qsa, args, world, rank):
+    """Chunked (prefill) scoring: args.chunk queries of one 50K-token request
+    at the chunk's last positions, against all of the request's blocks."""
+    spec = synth.spec_for(1)
+    g = synth.make_inputs(spec, device="cuda")
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    kc = torch.zeros((1, spec.max_blocks(), spec.n_idx_heads, spec.head_dim), dtype=torch.bfloat16, device="cuda")
+    qsa.compress_keys(d, g["idx_keys"], g["q_pos"], kc, ws)
+    n = args.chunk
+    L = spec.first_pos[0]
+    qi = synth.normal_bf16((1, n, spec.n_idx_heads, spec.head_dim), spec.seed + 77, device="cuda")
+    qp = torch.tensor([[L - (n - 1 - i) for i in range(n)]], dtype=torch.int32, device="cuda")
+    sc = torch.empty((1, n, spec.max_blocks()), dtype=torch.float32, device="cuda")
+    call = lambda: qsa.score_chunk(d, qi, kc, qp, sc, ws)
+    call()
+    status, info = qsa.check_errors(ws)
+    if status != qsa.OK:
+        raise RuntimeError(f"device error in chunked scoring: {info}")
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = None if args.no_flush else torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    ms_list = timed(call, args.steps, flush, torch.cuda.current_stream())
+    ms = max_over_ranks(sum(ms_list) / len(ms_list), world)
+    nf = [(int(p) + 1) // 4 for p in qp[0].tolist()]
+    b_out = sum(nf) * 4
+    b_kc = max(nf) * spec.n_idx_heads * spec.head_dim * 2
+    flops = 2 * sum(nf) * spec.n_idx_heads * spec.head_dim
+    if rank == 0:
+        print(json.dumps({"metric": "QSA chunked (prefill) scoring", "workload": f"b1-ctx{L}-chunk{n}",
+                          "latency_us": round(ms * 1e3, 2),
+                          "latency_us_p10_p50_p90": [round(float(np.percentile(ms_list, q)) * 1e3, 2)
+                                                     for q in (10, 50, 90)],
+                          "value": round((b_out + b_kc) * world / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
+                          "bytes": {"scores_written": b_out, "keys_read_once": b_kc},
+                          "tflops": round(flops * world / (ms * 1e-3) / 1e12, 2),
+                          "l2": "no flush (warm)" if flush is None else "flushed before every call"}))
+
+
 def run_ours(args, world, rank):
     qsa = build_lib()
+    if args.chunk:
+        return run_chunk(qsa, args, world, rank)
     spec = synth.spec_for(args.config, batch=args.batch, ctx=args.ctx)
     st = make_gpu_state(qsa, spec)
     if args.paged_kc:

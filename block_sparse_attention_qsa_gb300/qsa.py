@@ -32,7 +32,7 @@ EXPORTS = (
     "qsa_abi_version", "qsa_status_str", "qsa_dims_default", "qsa_workspace_size",
     "qsa_workspace_init", "qsa_compress_keys", "qsa_score", "qsa_topk", "qsa_sparse_attn",
     "qsa_decode", "qsa_check_errors", "qsa_sparse_attn_noalloc", "qsa_draft_attn",
-    "qsa_compress_keys_paged", "qsa_score_paged", "qsa_decode_paged",
+    "qsa_compress_keys_paged", "qsa_score_paged", "qsa_decode_paged", "qsa_score_chunk",
 )
 
 MAX_DRAFT_GAP = 64  # QSA_MAX_DRAFT_GAP
@@ -81,6 +81,7 @@ def _load() -> ctypes.CDLL:
         "qsa_compress_keys_paged": (I, [D, P, P, P, P, P, P, SZ, P]),
         "qsa_score_paged": (I, [D, P, P, P, P, P, P, SZ, P]),
         "qsa_decode_paged": (I, [D, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+        "qsa_score_chunk": (I, [D, ctypes.c_int32, P, P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -237,6 +238,21 @@ def sparse_attn_noalloc(d: Dims, q, k_cache, v_cache, k_scale, v_scale, page_tab
     _check(lib.qsa_sparse_attn_noalloc(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                        _ptr(v_scale), _ptr(page_table), _ptr(sel_pos), _ptr(q_pos), _ptr(out),
                                        _stream(stream)), "qsa_sparse_attn_noalloc")
+
+
+def score_chunk(d: Dims, q_idx, kc, q_pos, scores, ws, stream=None):
+    """Scores of a chunk of many queries per request (q_idx [B][n_chunk][H][128],
+    q_pos [B][n_chunk], scores [B][n_chunk][max_blocks])."""
+    if q_idx.dim() != 4:
+        raise ValueError("q_idx must be [B][n_chunk][H][128]")
+    n_chunk = int(q_idx.shape[1])
+    _want(q_idx, "q_idx", (d.batch, n_chunk, d.n_idx_heads, d.idx_dim), torch.bfloat16)
+    _want(kc, "kc", (d.batch, d.max_blocks, d.n_idx_heads, d.idx_dim), torch.bfloat16)
+    _want(q_pos, "q_pos", (d.batch, n_chunk), torch.int32)
+    _want(scores, "scores", (d.batch, n_chunk, d.max_blocks), torch.float32)
+    w, n = _ws(d, ws)
+    _check(lib.qsa_score_chunk(ctypes.byref(d), n_chunk, _ptr(q_idx), _ptr(kc), _ptr(q_pos), _ptr(scores), w, n,
+                               _stream(stream)), "qsa_score_chunk")
 
 
 def _want_kc_cache(d: Dims, kc_cache):

@@ -85,6 +85,9 @@ extern "C" {
  * reuses (qsa_draft_attn). */
 #define QSA_MAX_DRAFT_GAP 64
 
+/* Most queries per request in one qsa_score_chunk call. */
+#define QSA_MAX_CHUNK 65536
+
 typedef enum {
   QSA_OK = 0,
   QSA_ERR_INVALID_ARG = 1, /* null pointer, bad size or stride */
@@ -210,6 +213,18 @@ qsa_status qsa_sparse_attn_noalloc(const qsa_dims* dims, const void* q, const vo
                                    const void* v_cache, const float* k_scale, const float* v_scale,
                                    const int32_t* page_table, const int32_t* sel_pos,
                                    const int32_t* q_pos, void* out, void* stream);
+
+/* Scoring a chunk of many queries per request (a prefill chunk) against the
+ * request's blocks: the score of step 1 (arex-research.com, section
+ * "四类优化", bullets 1-2) for n_chunk queries at once, which makes it a dense
+ * BF16 product over (query, block) pairs. dims gives batch, n_idx_heads,
+ * max_blocks (its n_q is not used). q_idx is [B][n_chunk][n_idx_heads][128]
+ * BF16, q_pos [B][n_chunk], kc as for qsa_score, scores
+ * [B][n_chunk][max_blocks] FP32: scores[r][i][b] = sum_h sum_d
+ * q_idx[r][i][h][d] * kc[r][b][h][d] in FP32 for b < (q_pos[r][i] + 1) / 4;
+ * other entries are not written. 1 <= n_chunk <= QSA_MAX_CHUNK. */
+qsa_status qsa_score_chunk(const qsa_dims* dims, int32_t n_chunk, const void* q_idx, const void* kc,
+                           const int32_t* q_pos, float* scores, void* ws, size_t ws_bytes, void* stream);
 
 /* Paged compressed keys (the pages place the selected history "in the
  * cache", 10100.com "第一处"; here the compressed keys live in the KV

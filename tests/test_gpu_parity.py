@@ -401,6 +401,69 @@ def _run_decode(qsa, spec, g):
 
 
 # --------------------------------------------------------------------------
+# chunked (prefill) scoring: many queries per request (qsa_score_chunk)
+# --------------------------------------------------------------------------
+
+def _chunk_case(qsa, spec, n_chunk, q_pos, seed):
+    inp = synth.make_inputs(spec)
+    g = _dev(inp)
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    kc = torch.zeros((spec.batch, spec.max_blocks(), spec.n_idx_heads, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.compress_keys(d, g["idx_keys"], g["q_pos"], kc, ws)
+    qi = synth.normal_bf16((spec.batch, n_chunk, spec.n_idx_heads, 128), seed, device="cuda")
+    qp = torch.tensor(q_pos, dtype=torch.int32, device="cuda")
+    sc = torch.full((spec.batch, n_chunk, spec.max_blocks()), float("nan"), device="cuda")
+    qsa.score_chunk(d, qi, kc, qp, sc, ws)
+    return sc.cpu().numpy(), bits(qi), bits(kc), ws
+
+
+@pytest.mark.parametrize("h", [1, 2, 4])
+def test_score_chunk_parity(qsa, h):
+    spec = small_spec([5003, 2900], n_q=1, n_idx_heads=h, seed=31 + h)
+    n_chunk = 150  # three query tiles, the last ragged
+    q_pos = [[max(0, spec.first_pos[r] - 3 * (n_chunk - 1 - i)) for i in range(n_chunk)] for r in range(2)]
+    q_pos[1][0] = 5  # a query with no full block yet... and one with 1
+    q_pos[1][1] = 4
+    sc, qi, kcb, ws = _chunk_case(qsa, spec, n_chunk, q_pos, 9001 + h)
+    _check_ok(qsa, ws)
+    for r in range(2):
+        for i in range(n_chunk):
+            p = q_pos[r][i]
+            n = O.n_full(p)
+            ref = O.score_row(qi[r, i], kcb[r], p)
+            got = sc[r, i, :n]
+            assert np.all(np.abs(got - ref) <= SCORE_RTOL * np.maximum(np.abs(ref), 1.0)), (r, i)
+            assert np.all(np.isnan(sc[r, i, n:])), (r, i)  # nothing written past the causal blocks
+
+
+def test_score_chunk_full_size_sampled(qsa):
+    spec = synth.spec_for(1)  # one request, 50,000-token context
+    n_chunk = 1024
+    L = spec.first_pos[0]
+    q_pos = [[L - (n_chunk - 1 - i) for i in range(n_chunk)]]
+    sc, qi, kcb, ws = _chunk_case(qsa, spec, n_chunk, q_pos, 9100)
+    _check_ok(qsa, ws)
+    for i in (0, 1, 63, 64, 511, 777, 1023):
+        p = q_pos[0][i]
+        n = O.n_full(p)
+        ref = O.score_row(qi[0, i], kcb[0], p)
+        assert np.all(np.abs(sc[0, i, :n] - ref) <= SCORE_RTOL * np.maximum(np.abs(ref), 1.0)), i
+
+
+def test_score_chunk_reports_a_bad_position(qsa):
+    spec = small_spec([3001], n_q=1, seed=33)
+    q_pos = [[-1] + [3001 - 40 + i for i in range(39)]]
+    sc, qi, kcb, ws = _chunk_case(qsa, spec, 40, q_pos, 9200)
+    st, info = qsa.check_errors(ws)
+    assert st == qsa.ERR_BAD_INDEX and info[0] == 1 and info[2] == 0, info
+    assert np.all(np.isnan(sc[0, 0]))
+    p = q_pos[0][5]
+    ref = O.score_row(qi[0, 5], kcb[0], p)
+    assert np.all(np.abs(sc[0, 5, :O.n_full(p)] - ref) <= SCORE_RTOL * np.maximum(np.abs(ref), 1.0))
+
+
+# --------------------------------------------------------------------------
 # compressed keys in the KV cache's pages (qsa_*_paged)
 # --------------------------------------------------------------------------
 
