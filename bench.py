@@ -403,7 +403,7 @@ def run_ours(args, world, rank):
     qsa = build_lib()
     if args.chunk:
         return run_chunk(qsa, args, world, rank)
-    spec = synth.spec_for(args.config, batch=args.batch, ctx=args.ctx)
+    spec = synth.spec_for(args.config, batch=args.batch, ctx=args.ctx, replica=rank)
     st = make_gpu_state(qsa, spec)
     if args.paged_kc:
         g = st["g"]

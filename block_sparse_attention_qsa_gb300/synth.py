@@ -194,7 +194,7 @@ def turn_growth_positions(batch: int, seed: int, first: int = 50000, per_turn: i
     return [first + per_turn * t for t in uint_below(batch, turns, seed)]
 
 
-def spec_for(config: int, batch: Optional[int] = None, ctx: Optional[int] = None) -> Spec:
+def spec_for(config: int, batch: Optional[int] = None, ctx: Optional[int] = None, replica: int = 0) -> Spec:
     """The five workloads of the decode / verify step, by number.
 
     0: batch 1, one query at position 4,098 (1,024 full blocks + a 3-token
@@ -206,7 +206,9 @@ def spec_for(config: int, batch: Optional[int] = None, ctx: Optional[int] = None
     4: batch ``batch`` x context ``ctx`` in {131,072, 262,144}, 4 verify
        queries, 4 index heads, FP8-E4M3 paged KV.
     """
-    seed = SEED_BASE + 1000 * config
+    # replica r of a multi-GPU run draws its own requests (its shard of the
+    # global batch) from the same distribution
+    seed = SEED_BASE + 1000 * config + 100_000 * replica
     if config == 0:
         return Spec("tiny-decode-b1-ctx4099", 1, 1, [4098], 1, "bf16", False, seed)
     if config == 1:
