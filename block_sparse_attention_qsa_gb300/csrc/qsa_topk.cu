@@ -659,8 +659,8 @@ cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q
                         int32_t* sel_blk, int32_t* sel_pos, int32_t* err, const int32_t* page_table,
                         int32_t* sel_row, cudaStream_t s, bool pdl) {
   const int rows = d.batch * d.n_q;
-  // shared memory: header + either the bitmap path's candidates and two
-  // bitmaps, or the long-row path's keys
+  // shared memory: the header, and the long-row path's keys (the register
+  // path keeps its keys in registers)
   const int mb = d.max_blocks;
   const int mb32 = (mb + 31) / 32 * 32;
   const int fast_cap = mb <= kTopK ? 0 : (mb32 < kFastCap ? mb32 : kFastCap);

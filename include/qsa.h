@@ -15,6 +15,11 @@
  *   4. sparse attention over the selected positions with a BF16 query and a
  *      BF16 or FP8-E4M3 KV cache (bullet 3); the three kernels are chained
  *      with programmatic dependent launch (bullet 4).
+ * Around the step: qsa_compress_keys (the compressed keys themselves),
+ * qsa_draft_attn (MTP draft steps reusing a selection), the *_paged entry
+ * points (compressed keys kept in the KV cache's pages), qsa_score_chunk
+ * (scoring a chunk of many queries per request) and qsa_sparse_attn_noalloc
+ * (attention without a caller workspace).
  *
  * Readings where the pages are silent:
  *   - full blocks of a query at position p: b < (p + 1) / 4; the unfilled
@@ -33,6 +38,8 @@
  *   q_idx      bf16  [batch][n_q][n_idx_heads][idx_dim]
  *   idx_keys   bf16  [batch][4 * max_blocks][n_idx_heads][idx_dim]
  *   kc         bf16  [batch][max_blocks][n_idx_heads][idx_dim]
+ *   kc_cache   bf16  [num_pages][page_size / 4][n_idx_heads][idx_dim]
+ *                                        (the *_paged entry points)
  *   q_pos      int32 [batch][n_q]        position of each query token; the
  *                                        query's own K/V is already cached
  *   scores     fp32  [batch][n_q][max_blocks]   (entries past a query's
@@ -132,7 +139,7 @@ const char* qsa_status_str(qsa_status s);
 void qsa_dims_default(qsa_dims* dims);
 
 /* Bytes of workspace the entry points need for `dims` on the current device.
- * The size depends on the device's SM count (it sizes split-KV scratch). */
+ * The size depends on the device's SM count (it sizes the attention partials). */
 qsa_status qsa_workspace_size(const qsa_dims* dims, size_t* bytes);
 
 /* Zero `ws` (ws_bytes bytes) on `stream`. Required once after allocating a

@@ -102,8 +102,8 @@ def test_binding_refuses_host_tensors(qsa):
 
 @no_device
 def test_noalloc_rejects_sizes_beyond_its_scratch(qsa):
-    # 300,000 requests x 4 queries x 2 KV heads: far more split-KV units than
-    # the 8 MiB static scratch holds
+    # 300,000 requests x 4 queries: far more resolved cache rows than the
+    # 16 MiB static scratch holds
     d = qsa.make_dims(300000, 4, 16, 1, 1)
     fake = ctypes.c_void_p(1 << 20)
     st = qsa.lib.qsa_sparse_attn_noalloc(ctypes.byref(d), fake, fake, fake, None, None, fake, fake, fake, fake,
