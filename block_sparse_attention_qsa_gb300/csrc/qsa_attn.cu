@@ -11,15 +11,17 @@
 // of selected positions form one stream of tiles, cut into equal contiguous
 // shares, one per resident 4-warp CTA, so every CTA does the same work and
 // the kernel has no wave tail. Within a tile every warp works alone on 16
-// positions: lane 4g + c holds positions g and g + 8. The selected K/V rows are random 256-byte (BF16) or 128-byte (FP8) rows, so the
+// positions (BF16; lane 4g + c holds positions g and g + 8) or 32 (FP8; g,
+// g + 8, g + 16, g + 24), so that a warp step moves 8 KB of K and V for either
+// cache type. The selected K/V rows are random 256-byte (BF16) or 128-byte (FP8) rows, so the
 // kernel is a gather: measured on GB300, 128-bit loads straight into
 // registers, with each warp reading whole rows, sustain a much higher share
 // of HBM bandwidth for such gathers than staging through shared memory. So K
 // and V never touch shared memory:
 //
 //  * S^T = K Q^T on the tensor cores (mma.sync m16n8k16, FP32 accumulate):
-//    the warp's 16 positions are the M rows, the KV group's 8 query heads the
-//    N columns. A lane's 16-byte loads of K rows
+//    each 16 of the warp's positions are the M rows of one mma, the KV
+//    group's 8 query heads the N columns. A lane's 16-byte loads of K rows
 //    are its A fragments directly, because the head dim is visited in a
 //    lane-dependent order that Q's B fragments follow too (a dot product does
 //    not depend on the order of its terms).
@@ -44,11 +46,13 @@
 namespace qsa {
 namespace {
 
-constexpr int kTile = 64;       // positions per CTA step: 4 warps of 16
+constexpr int kTile = 64;       // BF16 positions per CTA step: 4 warps of 16 (FP8: 4 of 32)
 // resident CTAs per SM: BF16 rows take twice the registers of FP8 codes
 // (two rows of K and V per lane: 64 registers against 32)
 template <bool FP8>
-constexpr int kCtasPerSm = FP8 ? 4 : 3;
+constexpr int kCtasPerSm = 3;
+template <bool FP8>
+constexpr int kRowsPerLane = FP8 ? 4 : 2;
 // Small batches: each CTA takes at least this many tiles, so a unit is cut
 // into at most 17 pieces and the merge of the last piece to arrive stays short
 // (measured at batch 1: 1 tile 35.1 us per step, 2 tiles 32.2, 4 tiles 33.5).
@@ -196,13 +200,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
   __shared__ float s_ml[96];
   __shared__ int s_last;
 
-  // 16 positions per warp step: lane 4g + c holds rows g and g + 8, all 16 M
-  // rows of the score mma and the full k of the PV mma
-  constexpr int POS = 16;
+  // positions per warp step: lane 4g + c holds rows g + 8k, k < R, so each
+  // pair of rows fills the 16 M rows of a score mma and the k of a PV mma.
+  // BF16: 2 rows (16 positions); FP8: 4 rows (32 positions), so that a step
+  // moves as many bytes for either cache type
+  constexpr int R = kRowsPerLane<FP8>;
+  constexpr int POS = 8 * R;
   constexpr int TILE = 4 * POS;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gq = lane >> 2, c4 = lane & 3;
-  const int ent = warp * POS + gq;  // this lane's position within a tile (FP8: and ent + 8)
+  const int ent = warp * POS + gq;  // this lane's first position within a tile (then ent + 8k)
   const int n_q_heads = a.n_kv * kGroup;
   const int P = a.page_size;
   using RR = RowRegs<FP8>;
@@ -245,19 +252,31 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
       }
     }
   };
-  const int e0 = load_entry(true, 0), e0h = load_entry(true, 8), g0 = L.g;
-  advance();
-  int e1 = load_entry(w0 + 1 < w1, 0), e1h = load_entry(w0 + 1 < w1, 8), g1 = L.g;
+  // this lane's rows of tile w: positions ent + 8k, k < R (R rows of 16-row mma tiles)
+  int e1[R];
+  int ri[R];
+  {
+    int e0[R];
+#pragma unroll
+    for (int k = 0; k < R; ++k) e0[k] = load_entry(true, 8 * k);
+    const int g0 = L.g;
+    advance();
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+      e1[k] = load_entry(w0 + 1 < w1, 8 * k);
+      ri[k] = e0[k] >= 0 ? e0[k] + g0 * P : -1;
+    }
+  }
+  int g1 = L.g;
   advance();
   long long wl = w0 + 2;  // tile of the cursor
 
-  RR kr, vr, krh, vrh;  // rows g and g + 8
-  int ri = e0 >= 0 ? e0 + g0 * P : -1;
-  int rih = e0h >= 0 ? e0h + g0 * P : -1;
-  kr.load(kbase + (size_t)max(ri, 0) * RR::kRowBytes, c4, ri >= 0);
-  vr.load(vbase + (size_t)max(ri, 0) * RR::kRowBytes, c4, ri >= 0);
-  krh.load(kbase + (size_t)max(rih, 0) * RR::kRowBytes, c4, rih >= 0);
-  vrh.load(vbase + (size_t)max(rih, 0) * RR::kRowBytes, c4, rih >= 0);
+  RR kr[R], vr[R];
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    kr[k].load(kbase + (size_t)max(ri[k], 0) * RR::kRowBytes, c4, ri[k] >= 0);
+    vr[k].load(vbase + (size_t)max(ri[k], 0) * RR::kRowBytes, c4, ri[k] >= 0);
+  }
 
   long long w = w0;
   for (int buf = 0;; buf ^= 1) {
@@ -304,40 +323,54 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
     for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
     for (int i = 0; i < seg; ++i, ++w) {
-      // S^T (POS positions x 8 heads)
-      float s[4] = {0.f, 0.f, 0.f, 0.f};
+      // S^T (POS positions x 8 heads): R / 2 mma tiles of 16 positions (rows 2j, 2j + 1)
+      float s[R / 2][4];
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        if constexpr (FP8) {
-          const uint32_t wl0 = kr.pr[ks], wh0 = krh.pr[ks];
-          mma16816<true>(s, e4m3x2_to_h2(wl0), e4m3x2_to_h2(wh0), e4m3x2_to_h2(wl0 >> 16), e4m3x2_to_h2(wh0 >> 16),
-                         qb[2 * ks], qb[2 * ks + 1]);
-        } else {
-          mma16816<false>(s, kr.pr[2 * ks], krh.pr[2 * ks], kr.pr[2 * ks + 1], krh.pr[2 * ks + 1], qb[2 * ks],
-                          qb[2 * ks + 1]);
+      for (int j = 0; j < R / 2; ++j) {
+        s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          if constexpr (FP8) {
+            const uint32_t wl0 = kr[2 * j].pr[ks], wh0 = kr[2 * j + 1].pr[ks];
+            mma16816<true>(s[j], e4m3x2_to_h2(wl0), e4m3x2_to_h2(wh0), e4m3x2_to_h2(wl0 >> 16),
+                           e4m3x2_to_h2(wh0 >> 16), qb[2 * ks], qb[2 * ks + 1]);
+          } else {
+            mma16816<false>(s[j], kr[2 * j].pr[2 * ks], kr[2 * j + 1].pr[2 * ks], kr[2 * j].pr[2 * ks + 1],
+                            kr[2 * j + 1].pr[2 * ks + 1], qb[2 * ks], qb[2 * ks + 1]);
+          }
         }
       }
-      const bool ok = ri >= 0, okh = rih >= 0;
+      bool ok[R];
+#pragma unroll
+      for (int k = 0; k < R; ++k) ok[k] = ri[k] >= 0;
       // the next tile of the share (this unit or the next): its K rows now
       const bool next = w + 1 < w1;
-      const int nri = e1 >= 0 ? e1 + g1 * P : -1;
-      const int nrih = e1h >= 0 ? e1h + g1 * P : -1;
-      e1 = load_entry(wl < w1, 0);
-      e1h = load_entry(wl < w1, 8);
+      int nri[R];
+#pragma unroll
+      for (int k = 0; k < R; ++k) {
+        nri[k] = e1[k] >= 0 ? e1[k] + g1 * P : -1;
+        e1[k] = load_entry(wl < w1, 8 * k);
+      }
       g1 = L.g;
       advance();
       ++wl;
       if (next) {
-        kr.load(kbase + (size_t)max(nri, 0) * RR::kRowBytes, c4, nri >= 0);
-        krh.load(kbase + (size_t)max(nrih, 0) * RR::kRowBytes, c4, nrih >= 0);
+#pragma unroll
+        for (int k = 0; k < R; ++k) kr[k].load(kbase + (size_t)max(nri[k], 0) * RR::kRowBytes, c4, nri[k] >= 0);
       }
-      // online softmax; s[0], s[1]: position gq, heads 2c4, 2c4 + 1; s[2], s[3]:
-      // position gq + 8
-      const float x0 = ok ? s[0] * scale_log2 : kNegInf;
-      const float x1 = ok ? s[1] * scale_log2 : kNegInf;
-      const float x2 = okh ? s[2] * scale_log2 : kNegInf;
-      const float x3 = okh ? s[3] * scale_log2 : kNegInf;
-      float mA = fmaxf(x0, x2), mB = fmaxf(x1, x3);
+      // online softmax; s[j][0], s[j][1]: row 2j (position ent + 16j), heads 2c4,
+      // 2c4 + 1; s[j][2], s[j][3]: row 2j + 1 (position ent + 16j + 8)
+      float x[R / 2][4];
+      float mA = kNegInf, mB = kNegInf;
+#pragma unroll
+      for (int j = 0; j < R / 2; ++j) {
+        x[j][0] = ok[2 * j] ? s[j][0] * scale_log2 : kNegInf;
+        x[j][1] = ok[2 * j] ? s[j][1] * scale_log2 : kNegInf;
+        x[j][2] = ok[2 * j + 1] ? s[j][2] * scale_log2 : kNegInf;
+        x[j][3] = ok[2 * j + 1] ? s[j][3] * scale_log2 : kNegInf;
+        mA = fmaxf(mA, fmaxf(x[j][0], x[j][2]));
+        mB = fmaxf(mB, fmaxf(x[j][1], x[j][3]));
+      }
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
         mA = fmaxf(mA, __shfl_xor_sync(kFull, mA, o));
@@ -346,10 +379,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
       const float nA = fmaxf(m_run[0], mA), nB = fmaxf(m_run[1], mB);
       const float bA = nA == kNegInf ? 0.f : nA, bB = nB == kNegInf ? 0.f : nB;
       const float alA = exp2f(m_run[0] - bA), alB = exp2f(m_run[1] - bB);
-      const float p0 = exp2f(x0 - bA), p1 = exp2f(x1 - bB);
-      const float p2 = exp2f(x2 - bA), p3 = exp2f(x3 - bB);
-      l_run[0] = l_run[0] * alA + (p0 + p2);
-      l_run[1] = l_run[1] * alB + (p1 + p3);
+      float sumA = 0.f, sumB = 0.f;
+      uint32_t pb[R];  // P^T fragments: row k's probabilities, transposed
+#pragma unroll
+      for (int j = 0; j < R / 2; ++j) {
+        const float p0 = exp2f(x[j][0] - bA), p1 = exp2f(x[j][1] - bB);
+        const float p2 = exp2f(x[j][2] - bA), p3 = exp2f(x[j][3] - bB);
+        sumA += p0 + p2;
+        sumB += p1 + p3;
+        pb[2 * j] = movt(pack2<FP8>(p0, p1));
+        pb[2 * j + 1] = movt(pack2<FP8>(p2, p3));
+      }
+      l_run[0] = l_run[0] * alA + sumA;
+      l_run[1] = l_run[1] * alB + sumB;
       m_run[0] = nA;
       m_run[1] = nB;
 #pragma unroll
@@ -359,27 +401,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
         acc[k][2] *= alA;
         acc[k][3] *= alB;
       }
-      // O^T += V^T P^T
-      const uint32_t pb = movt(pack2<FP8>(p0, p1)), pbh = movt(pack2<FP8>(p2, p3));
-      if constexpr (FP8) {
+      // O^T += V^T P^T, one k step of 16 positions per pair of rows
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const uint32_t wl0 = vr.pr[mt], wh0 = vrh.pr[mt];
-          mma16816<true>(acc[mt], movt(e4m3x2_to_h2(wl0)), movt(e4m3x2_to_h2(wl0 >> 16)), movt(e4m3x2_to_h2(wh0)),
-                         movt(e4m3x2_to_h2(wh0 >> 16)), pb, pbh);
+      for (int j = 0; j < R / 2; ++j) {
+        if constexpr (FP8) {
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            const uint32_t wl0 = vr[2 * j].pr[mt], wh0 = vr[2 * j + 1].pr[mt];
+            mma16816<true>(acc[mt], movt(e4m3x2_to_h2(wl0)), movt(e4m3x2_to_h2(wl0 >> 16)),
+                           movt(e4m3x2_to_h2(wh0)), movt(e4m3x2_to_h2(wh0 >> 16)), pb[2 * j], pb[2 * j + 1]);
+          }
+        } else {
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt)
+            mma16816<false>(acc[mt], movt(vr[2 * j].pr[2 * mt]), movt(vr[2 * j].pr[2 * mt + 1]),
+                            movt(vr[2 * j + 1].pr[2 * mt]), movt(vr[2 * j + 1].pr[2 * mt + 1]), pb[2 * j],
+                            pb[2 * j + 1]);
         }
-      } else {
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
-          mma16816<false>(acc[mt], movt(vr.pr[2 * mt]), movt(vr.pr[2 * mt + 1]), movt(vrh.pr[2 * mt]),
-                          movt(vrh.pr[2 * mt + 1]), pb, pbh);
       }
       if (next) {
-        vr.load(vbase + (size_t)max(nri, 0) * RR::kRowBytes, c4, nri >= 0);
-        vrh.load(vbase + (size_t)max(nrih, 0) * RR::kRowBytes, c4, nrih >= 0);
+#pragma unroll
+        for (int k = 0; k < R; ++k) vr[k].load(vbase + (size_t)max(nri[k], 0) * RR::kRowBytes, c4, nri[k] >= 0);
       }
-      ri = nri;
-      rih = nrih;
+#pragma unroll
+      for (int k = 0; k < R; ++k) ri[k] = nri[k];
     }
 
     // ---- merge the 4 warps (the next unit's first K/V rows are in flight) ----
@@ -610,7 +655,8 @@ int page_shift_of(int page_size) {
 AttnPlan attn_plan(const qsa_dims& d, int num_sms) {
   AttnPlan pl;
   pl.units = d.batch * d.n_q * d.n_kv_heads;
-  pl.tiles = (d.width + kTile - 1) / kTile;
+  const int tile = d.kv_dtype == QSA_KV_FP8_E4M3 ? 2 * kTile : kTile;
+  pl.tiles = (d.width + tile - 1) / tile;
   const long long total = (long long)pl.units * pl.tiles;
   const long long resident =
       (long long)(d.kv_dtype == QSA_KV_FP8_E4M3 ? kCtasPerSm<true> : kCtasPerSm<false>) * num_sms;
