@@ -127,6 +127,31 @@ def test_score_parity(qsa, name):
             assert np.all(np.isnan(got[r, j, nb:]))  # nothing written past the full blocks
 
 
+@pytest.mark.parametrize("config,batch,ctx", [(2, 32, None), (4, 8, 131072)])
+def test_score_full_size_every_row(qsa, config, batch, ctx):
+    # every score of every row at a full batch, written once and nowhere else,
+    # on repeated calls through one workspace
+    spec = synth.spec_for(config, batch=batch, ctx=ctx)
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    H, nb_max = spec.n_idx_heads, spec.max_blocks()
+    q_idx = synth.normal_bf16((spec.batch, spec.n_q, H, 128), spec.seed + 11, "cuda")
+    kc = synth.normal_bf16((spec.batch, nb_max, H, 128), spec.seed + 12, "cuda")
+    q_pos = torch.tensor(spec.q_pos(), dtype=torch.int32, device="cuda")
+    scores = torch.full((spec.batch, spec.n_q, nb_max), float("nan"), device="cuda")
+    for _ in range(2):
+        qsa.score(d, q_idx, kc, q_pos, scores, ws)
+    _check_ok(qsa, ws)
+    qb, kb, got = bits(q_idx), bits(kc), scores.cpu().numpy()
+    for r in range(spec.batch):
+        for j in range(spec.n_q):
+            ref = O.score_row(qb[r, j], kb[r], spec.q_pos()[r][j])
+            nb = ref.shape[0]
+            err = np.abs(got[r, j, :nb].astype(np.float64) - ref) / np.maximum(np.abs(ref), 1.0)
+            assert err.max() <= SCORE_RTOL, (r, j, err.max())
+            assert np.all(np.isnan(got[r, j, nb:]))
+
+
 def _score_rows(kind, n, seed):
     rng = np.random.default_rng(seed)
     if kind == "normal":
