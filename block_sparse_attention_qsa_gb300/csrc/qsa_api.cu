@@ -204,6 +204,7 @@ qsa_status qsa_score_chunk(const qsa_dims* dims, int32_t n_chunk, const void* q_
   if (!q_idx || !kc || !q_pos || !scores) return QSA_ERR_INVALID_ARG;
   if (!aligned16(q_idx) || !aligned16(kc)) return QSA_ERR_INVALID_ARG;
   if ((long long)dims->batch * n_chunk * dims->max_blocks >= (1LL << 40)) return QSA_ERR_UNSUPPORTED;
+  if (dims->batch > 65535) return QSA_ERR_UNSUPPORTED;  // one grid row (z) per request
   if ((st = check_ws(dims, ws, ws_bytes, nullptr)) != QSA_OK) return st;
   return from_cuda(launch_score_chunk(*dims, n_chunk, static_cast<const __nv_bfloat16*>(q_idx),
                                       static_cast<const __nv_bfloat16*>(kc), q_pos, scores, err_word(ws),

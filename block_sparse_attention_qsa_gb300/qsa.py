@@ -36,6 +36,7 @@ EXPORTS = (
 )
 
 MAX_DRAFT_GAP = 64  # QSA_MAX_DRAFT_GAP
+MAX_CHUNK = 65536  # QSA_MAX_CHUNK
 
 
 class QSAError(RuntimeError):

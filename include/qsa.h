@@ -229,7 +229,8 @@ qsa_status qsa_sparse_attn_noalloc(const qsa_dims* dims, const void* q, const vo
  * BF16, q_pos [B][n_chunk], kc as for qsa_score, scores
  * [B][n_chunk][max_blocks] FP32: scores[r][i][b] = sum_h sum_d
  * q_idx[r][i][h][d] * kc[r][b][h][d] in FP32 for b < (q_pos[r][i] + 1) / 4;
- * other entries are not written. 1 <= n_chunk <= QSA_MAX_CHUNK. */
+ * other entries are not written. 1 <= n_chunk <= QSA_MAX_CHUNK and batch <=
+ * 65,535, else QSA_ERR_INVALID_ARG / QSA_ERR_UNSUPPORTED before any launch. */
 qsa_status qsa_score_chunk(const qsa_dims* dims, int32_t n_chunk, const void* q_idx, const void* kc,
                            const int32_t* q_pos, float* scores, void* ws, size_t ws_bytes, void* stream);
 

@@ -39,6 +39,8 @@ def test_draft_gap_matches_the_header(qsa):
     txt = open(os.path.join(ROOT, "include", "qsa.h")).read()
     m = re.search(r"#define QSA_MAX_DRAFT_GAP (\d+)", txt)
     assert m and int(m.group(1)) == qsa.MAX_DRAFT_GAP
+    m = re.search(r"#define QSA_MAX_CHUNK (\d+)", txt)
+    assert m and int(m.group(1)) == qsa.MAX_CHUNK
 
 
 def test_abi_version_and_status_strings(qsa):
@@ -89,6 +91,14 @@ def test_workspace_size_and_rejections_need_no_gpu(qsa):
     assert qsa.lib.qsa_topk(ctypes.byref(d), fake, fake, fake, fake, None, n.value, None) == qsa.ERR_WORKSPACE
     assert qsa.lib.qsa_topk(ctypes.byref(d), fake, fake, fake, fake, ctypes.c_void_p((1 << 20) + 8), n.value,
                             None) == qsa.ERR_WORKSPACE
+    # chunked scoring: chunk length and batch limits
+    assert qsa.lib.qsa_score_chunk(ctypes.byref(d), 0, fake, fake, fake, fake, fake, n.value,
+                                   None) == qsa.ERR_INVALID_ARG
+    assert qsa.lib.qsa_score_chunk(ctypes.byref(d), qsa.MAX_CHUNK + 1, fake, fake, fake, fake, fake, n.value,
+                                   None) == qsa.ERR_INVALID_ARG
+    big = qsa.make_dims(65536, 1, 4, 1, 1)
+    assert qsa.lib.qsa_score_chunk(ctypes.byref(big), 1, fake, fake, fake, fake, fake, 1 << 40,
+                                   None) == qsa.ERR_UNSUPPORTED
 
 
 def test_binding_refuses_host_tensors(qsa):
