@@ -37,10 +37,6 @@ WsLayout ws_layout(const qsa_dims& d, int num_sms) {
   off = align_up(off + (size_t)grid_max * 2 * kPartFloats * sizeof(float), 256);
   w.scores = off;
   off = align_up(off + rows * d.max_blocks * sizeof(float), 256);
-  w.sel_blk = off;
-  off = align_up(off + rows * kTopK * sizeof(int32_t), 256);
-  w.sel_pos = off;
-  off = align_up(off + rows * kWidth * sizeof(int32_t), 256);
   w.sel_row = off;
   off = align_up(off + rows * kDraftWidth * sizeof(int32_t), 256);
   w.total = off;
@@ -264,14 +260,13 @@ qsa_status decode_impl(const qsa_dims* dims, const void* q_idx, const void* kc, 
   if ((st = check_ws(dims, ws, ws_bytes, &w)) != QSA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* sc = scores ? scores : at<float>(ws, w.scores);
-  int32_t* sb = sel_blk ? sel_blk : at<int32_t>(ws, w.sel_blk);
-  int32_t* spos = sel_pos ? sel_pos : at<int32_t>(ws, w.sel_pos);
   cudaError_t e = launch_score(*dims, static_cast<const __nv_bfloat16*>(q_idx),
                                static_cast<const __nv_bfloat16*>(kc), q_pos, sc, err_word(ws), s, false,
                                kc_paged ? page_table : nullptr);
   if (e != cudaSuccess) return QSA_ERR_CUDA;
   int32_t* srow = at<int32_t>(ws, w.sel_row);
-  e = launch_topk(*dims, sc, q_pos, sb, spos, err_word(ws), page_table, srow, s, true);
+  // block ids and positions only when the caller asked for them; attention needs the cache rows
+  e = launch_topk(*dims, sc, q_pos, sel_blk, sel_pos, err_word(ws), page_table, srow, s, true);
   if (e != cudaSuccess) return QSA_ERR_CUDA;
   const AttnPlan pl{w.units, w.tiles, w.grid};
   e = launch_attn(*dims, q, k_cache, v_cache, k_scale, v_scale, srow, out, at<int32_t>(ws, w.tickets),

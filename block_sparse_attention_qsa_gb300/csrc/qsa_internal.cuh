@@ -35,15 +35,13 @@ constexpr int kDraftWidth = kWidth + kMaxDraftGap;
 //   tickets            int32 [units]           arrival counters of split units
 //   partials           float [grid][2][kPartFloats]  pieces of units split between CTAs
 //   scores (decode)    float [B][n_q][max_blocks]
-//   sel_blk (decode)   int32 [B][n_q][512]
-//   sel_pos (decode)   int32 [B][n_q][2051]
 //   sel_row            int32 [B][n_q][2051 + kMaxDraftGap]  cache row (KV head 0) of each
 //                      selected position (row stride 2051, or 2051 + kMaxDraftGap for draft steps)
 // ---------------------------------------------------------------------------
 constexpr int kPartFloats = 2 * kGroup + kGroup * kDim;  // m[8], l[8], acc[8][128]
 
 struct WsLayout {
-  size_t tickets, partials, scores, sel_blk, sel_pos, sel_row, total;
+  size_t tickets, partials, scores, sel_row, total;
   int units, tiles, grid;
 };
 

@@ -310,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
   for (int row = blockIdx.x; row < rows; row += gridDim.x) {
     if (row != (int)blockIdx.x) stage_row(row);
     __syncthreads();  // staged page table and zeroed histograms
-    int32_t* ob = sel_blk + (size_t)row * kTopK;
-    int32_t* op = sel_pos + (size_t)row * kWidth;
+    int32_t* ob = sel_blk ? sel_blk + (size_t)row * kTopK : nullptr;
+    int32_t* op = sel_pos ? sel_pos + (size_t)row * kWidth : nullptr;
     int32_t* orow = ro.page_table ? ro.sel_row + (size_t)row * kWidth : nullptr;
     const int32_t* pt = pt_ok ? pt_s : nullptr;
     const int r = row / n_q, j = row - r * n_q;
@@ -320,8 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
     if (!p_ok || n <= kTopK) {
       if (!p_ok && tid == 0) record_error(err, kErrQueryPos, r, j, p);
       // every full block is kept (positions 0..p), or nothing for a bad position
-      for (int i = tid; i < kTopK; i += kThreads) ob[i] = i < n ? i : -1;
-      for (int i = tid; i < kWidth; i += kThreads) op[i] = (p_ok && i <= p) ? i : -1;
+      if (ob)
+        for (int i = tid; i < kTopK; i += kThreads) ob[i] = i < n ? i : -1;
+      if (op)
+        for (int i = tid; i < kWidth; i += kThreads) op[i] = (p_ok && i <= p) ? i : -1;
       if (orow)
         for (int i = tid; i < kWidth; i += kThreads) orow[i] = (p_ok && i <= p) ? row_of(ro, pt, r, i, err, j) : -1;
       __syncthreads();  // shared memory is reused by the next row
@@ -409,14 +411,16 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
     }
     __syncthreads();  // the selection list is complete
     // outputs, coalesced: block ids, their positions (then the unfilled block's), cache rows
-    for (int i = tid; i < kTopK; i += kThreads) ob[i] = blk[i];
-    for (int i = tid; i < kWidth; i += kThreads) {
-      int pos;
-      if (i < kBlock * kTopK) pos = kBlock * blk[i >> 2] + (i & 3);
-      else pos = (i - kBlock * kTopK < npart) ? kBlock * n + (i - kBlock * kTopK) : -1;
-      op[i] = pos;
-      if (orow) orow[i] = pos < 0 ? -1 : row_of(ro, pt, r, pos, err, j);
-    }
+    if (ob)
+      for (int i = tid; i < kTopK; i += kThreads) ob[i] = blk[i];
+    if (op || orow)
+      for (int i = tid; i < kWidth; i += kThreads) {
+        int pos;
+        if (i < kBlock * kTopK) pos = kBlock * blk[i >> 2] + (i & 3);
+        else pos = (i - kBlock * kTopK < npart) ? kBlock * n + (i - kBlock * kTopK) : -1;
+        if (op) op[i] = pos;
+        if (orow) orow[i] = pos < 0 ? -1 : row_of(ro, pt, r, pos, err, j);
+      }
     for (int i = tid; i < 2 * kHistBins; i += kThreads) hist[i] = 0;
     __syncthreads();  // shared memory is reused by the next row
   }
@@ -493,8 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const float* 
   pdl_trigger();
   __syncthreads();
 
-  int32_t* ob = sel_blk + (size_t)row * kTopK;
-  int32_t* op = sel_pos + (size_t)row * kWidth;
+  int32_t* ob = sel_blk ? sel_blk + (size_t)row * kTopK : nullptr;
+  int32_t* op = sel_pos ? sel_pos + (size_t)row * kWidth : nullptr;
   int32_t* orow = ro.page_table ? ro.sel_row + (size_t)row * kWidth : nullptr;
   const int32_t* pt = pt_ok ? pt_s : nullptr;
   const bool p_ok = p >= 0 && n_full_of(p) <= max_blocks && (!orow || (p >> ro.page_shift) < ro.max_pages);
@@ -502,8 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const float* 
   if (!p_ok || n <= kTopK) {
     if (crank == 0) {
       if (!p_ok && tid == 0) record_error(err, kErrQueryPos, r, j, p);
-      for (int i = tid; i < kTopK; i += kThreads) ob[i] = i < n ? i : -1;
-      for (int i = tid; i < kWidth; i += kThreads) op[i] = (p_ok && i <= p) ? i : -1;
+      if (ob)
+        for (int i = tid; i < kTopK; i += kThreads) ob[i] = i < n ? i : -1;
+      if (op)
+        for (int i = tid; i < kWidth; i += kThreads) op[i] = (p_ok && i <= p) ? i : -1;
       if (orow)
         for (int i = tid; i < kWidth; i += kThreads) orow[i] = (p_ok && i <= p) ? row_of(ro, pt, r, i, err, j) : -1;
     }
@@ -610,12 +616,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const float* 
     const int e = __ffs(pick) - 1;
     if (slot < (uint32_t)kTopK) {  // exactly kTopK; the bound is a guard
       const int b = v0 + e;
-      ob[slot] = b;
+      if (ob) ob[slot] = b;
       const int pos = kBlock * b;
       const int base = orow ? row_of(ro, pt, r, pos, err, j) : 0;  // a block never straddles a page
 #pragma unroll
       for (int k = 0; k < kBlock; ++k) {
-        op[kBlock * slot + k] = pos + k;
+        if (op) op[kBlock * slot + k] = pos + k;
         if (orow) orow[kBlock * slot + k] = base < 0 ? -1 : base + k;
       }
     }
@@ -624,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const float* 
   }
   if (crank == 0 && tid < kBlock - 1) {
     const int pos = tid < npart ? kBlock * n + tid : -1;
-    op[kBlock * kTopK + tid] = pos;
+    if (op) op[kBlock * kTopK + tid] = pos;
     if (orow) orow[kBlock * kTopK + tid] = pos < 0 ? -1 : row_of(ro, pt, r, pos, err, j);
   }
   cluster_sync();  // no CTA leaves while another may still read its counts

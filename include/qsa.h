@@ -190,7 +190,8 @@ qsa_status qsa_sparse_attn(const qsa_dims* dims, const void* q, const void* k_ca
 /* The fused step (bullet 4: "QSA logits -> select -> attention" chained with
  * programmatic dependent launch): qsa_score, qsa_topk and qsa_sparse_attn
  * back to back on `stream`. scores, sel_blk and sel_pos are optional outputs:
- * NULL keeps them in the workspace. */
+ * with NULL the scores stay in the workspace and the block ids and positions
+ * are not written (attention reads the cache rows the selector writes). */
 qsa_status qsa_decode(const qsa_dims* dims, const void* q_idx, const void* kc, const void* q,
                       const void* k_cache, const void* v_cache, const float* k_scale,
                       const float* v_scale, const int32_t* page_table, const int32_t* q_pos,

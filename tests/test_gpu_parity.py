@@ -61,6 +61,9 @@ SPECS = {
     "b1-nq1-h2": lambda: small_spec([5003], n_q=1, n_idx_heads=2, seed=7),
     "b2-nq3-h3": lambda: small_spec([2100, 3333], n_q=3, n_idx_heads=3, seed=8),
     "b2-nq2-h1-fp8": lambda: small_spec([9000, 2050], n_q=2, kv_dtype="fp8", seed=9),
+    # other page sizes: 16-token pages (a block of 4 tokens is a quarter page) and 256-token pages
+    "b2-p16-fp8": lambda: synth.Spec("small-p16", 2, 4, [2600, 999], 1, "fp8", True, 10, page_size=16),
+    "b2-p256-nq2-h2": lambda: synth.Spec("small-p256", 2, 2, [4000, 2301], 2, "bf16", True, 11, page_size=256),
 }
 
 
