@@ -39,8 +39,6 @@
 // publishes (max, sum, acc) pieces to the workspace and the last piece to
 // arrive, counted by an atomic ticket, merges them and resets the ticket, so
 // there is no spin-wait anywhere.
-#include <cuda_fp8.h>
-
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -115,10 +113,13 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
-// two E4M3 codes (low byte first) -> FP16x2, exact
-__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// four E4M3 codes (bytes 0-3 of w) -> FP16x2 of codes 0, 1 (lo) and of codes
+// 2, 3 (hi), exact: the word's two halves go straight to the hardware
+// conversion, with no masking, shifting or repacking around it
+__device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 // BF16 pair -> FP16 pair (Q of the FP8 path)
@@ -331,9 +332,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           if constexpr (FP8) {
-            const uint32_t wl0 = kr[2 * j].pr[ks], wh0 = kr[2 * j + 1].pr[ks];
-            mma16816<true>(s[j], e4m3x2_to_h2(wl0), e4m3x2_to_h2(wh0), e4m3x2_to_h2(wl0 >> 16),
-                           e4m3x2_to_h2(wh0 >> 16), qb[2 * ks], qb[2 * ks + 1]);
+            uint32_t a0, a1, a2, a3;
+            e4m3x4_to_h2x2(kr[2 * j].pr[ks], a0, a2);
+            e4m3x4_to_h2x2(kr[2 * j + 1].pr[ks], a1, a3);
+            mma16816<true>(s[j], a0, a1, a2, a3, qb[2 * ks], qb[2 * ks + 1]);
           } else {
             mma16816<false>(s[j], kr[2 * j].pr[2 * ks], kr[2 * j + 1].pr[2 * ks], kr[2 * j].pr[2 * ks + 1],
                             kr[2 * j + 1].pr[2 * ks + 1], qb[2 * ks], qb[2 * ks + 1]);
@@ -407,9 +409,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
         if constexpr (FP8) {
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
-            const uint32_t wl0 = vr[2 * j].pr[mt], wh0 = vr[2 * j + 1].pr[mt];
-            mma16816<true>(acc[mt], movt(e4m3x2_to_h2(wl0)), movt(e4m3x2_to_h2(wl0 >> 16)),
-                           movt(e4m3x2_to_h2(wh0)), movt(e4m3x2_to_h2(wh0 >> 16)), pb[2 * j], pb[2 * j + 1]);
+            uint32_t v0, v1, v2, v3;
+            e4m3x4_to_h2x2(vr[2 * j].pr[mt], v0, v1);
+            e4m3x4_to_h2x2(vr[2 * j + 1].pr[mt], v2, v3);
+            mma16816<true>(acc[mt], movt(v0), movt(v1), movt(v2), movt(v3), pb[2 * j], pb[2 * j + 1]);
           }
         } else {
 #pragma unroll
