@@ -76,6 +76,15 @@ __device__ __forceinline__ int ld_issue(const int32_t* p) {
   return v;
 }
 
+// 2^x on the special-function unit (the PTX ex2.approx.ftz instruction:
+// relative error about 2^-22, results below the normal range flushed to zero,
+// 2^-inf = 0). Used for the per-step softmax terms, whose arguments are <= 0.
+__device__ __forceinline__ float exp2_sfu(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // 8x8 transpose of 16-bit elements held one pair per lane (lane 4g + c holds
 // row g, columns 2c and 2c+1).
 __device__ __forceinline__ uint32_t movt(uint32_t x) {
@@ -380,13 +389,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
       }
       const float nA = fmaxf(m_run[0], mA), nB = fmaxf(m_run[1], mB);
       const float bA = nA == kNegInf ? 0.f : nA, bB = nB == kNegInf ? 0.f : nB;
-      const float alA = exp2f(m_run[0] - bA), alB = exp2f(m_run[1] - bB);
+      const float alA = exp2_sfu(m_run[0] - bA), alB = exp2_sfu(m_run[1] - bB);
+      // the accumulators need rescaling only when a running maximum moved (once
+      // the first tiles are in, rarely); an unmoved -inf maximum means nothing
+      // has been accumulated yet
+      const bool moved = !__all_sync(kFull, nA == m_run[0] && nB == m_run[1]);
       float sumA = 0.f, sumB = 0.f;
       uint32_t pb[R];  // P^T fragments: row k's probabilities, transposed
 #pragma unroll
       for (int j = 0; j < R / 2; ++j) {
-        const float p0 = exp2f(x[j][0] - bA), p1 = exp2f(x[j][1] - bB);
-        const float p2 = exp2f(x[j][2] - bA), p3 = exp2f(x[j][3] - bB);
+        const float p0 = exp2_sfu(x[j][0] - bA), p1 = exp2_sfu(x[j][1] - bB);
+        const float p2 = exp2_sfu(x[j][2] - bA), p3 = exp2_sfu(x[j][3] - bB);
         sumA += p0 + p2;
         sumB += p1 + p3;
         pb[2 * j] = movt(pack2<FP8>(p0, p1));
@@ -396,12 +409,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
       l_run[1] = l_run[1] * alB + sumB;
       m_run[0] = nA;
       m_run[1] = nB;
+      if (moved) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        acc[k][0] *= alA;
-        acc[k][1] *= alB;
-        acc[k][2] *= alA;
-        acc[k][3] *= alB;
+        for (int k = 0; k < 8; ++k) {
+          acc[k][0] *= alA;
+          acc[k][1] *= alB;
+          acc[k][2] *= alA;
+          acc[k][3] *= alB;
+        }
       }
       // O^T += V^T P^T, one k step of 16 positions per pair of rows
 #pragma unroll
