@@ -239,6 +239,33 @@ qsa_status qsa_sparse_attn(const qsa_dims* dims, const void* q, const void* k_ca
                                at<int32_t>(ws, w.tickets), at<float>(ws, w.partials), pl, s, true));
 }
 
+qsa_status qsa_resolve(const qsa_dims* dims, const int32_t* sel_pos, const int32_t* q_pos,
+                       const int32_t* page_table, int32_t* sel_row, void* ws, size_t ws_bytes, void* stream) {
+  qsa_status st = check_dims(dims);
+  if (st != QSA_OK) return st;
+  if (!sel_pos || !q_pos || !page_table || !sel_row) return QSA_ERR_INVALID_ARG;
+  if ((st = check_ws(dims, ws, ws_bytes, nullptr)) != QSA_OK) return st;
+  return from_cuda(launch_resolve(*dims, sel_pos, q_pos, page_table, sel_row, err_word(ws),
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+qsa_status qsa_sparse_attn_rows(const qsa_dims* dims, const void* q, const void* k_cache, const void* v_cache,
+                                const float* k_scale, const float* v_scale, const int32_t* sel_row, void* out,
+                                void* ws, size_t ws_bytes, void* stream) {
+  qsa_status st = check_dims(dims);
+  if (st != QSA_OK) return st;
+  if (!q || !k_cache || !v_cache || !sel_row || !out) return QSA_ERR_INVALID_ARG;
+  if (dims->kv_dtype == QSA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(q) & 3u))
+    return QSA_ERR_INVALID_ARG;
+  WsLayout w;
+  if ((st = check_ws(dims, ws, ws_bytes, &w)) != QSA_OK) return st;
+  const AttnPlan pl{w.units, w.tiles, w.grid};
+  return from_cuda(launch_attn(*dims, q, k_cache, v_cache, k_scale, v_scale, sel_row, out,
+                               at<int32_t>(ws, w.tickets), at<float>(ws, w.partials), pl,
+                               static_cast<cudaStream_t>(stream), true));
+}
+
 }  // extern "C"
 
 namespace {

@@ -182,6 +182,7 @@ struct AttnArgs {
   const float* k_scale;
   const float* v_scale;
   const int32_t* sel_row;  // cache row (KV head 0) of every selected position, -1 for none
+  int row_lim;             // a KV-head-0 row r is used only if 0 <= r < row_lim (all heads in the cache)
   __nv_bfloat16* out;
   int32_t* tickets;
   float* partials;
@@ -274,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
 #pragma unroll
     for (int k = 0; k < R; ++k) {
       e1[k] = load_entry(w0 + 1 < w1, 8 * k);
-      ri[k] = e0[k] >= 0 ? e0[k] + g0 * P : -1;
+      ri[k] = (unsigned)e0[k] < (unsigned)a.row_lim ? e0[k] + g0 * P : -1;
     }
   }
   int g1 = L.g;
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
       int nri[R];
 #pragma unroll
       for (int k = 0; k < R; ++k) {
-        nri[k] = e1[k] >= 0 ? e1[k] + g1 * P : -1;
+        nri[k] = (unsigned)e1[k] < (unsigned)a.row_lim ? e1[k] + g1 * P : -1;
         e1[k] = load_entry(wl < w1, 8 * k);
       }
       g1 = L.g;
@@ -708,6 +709,8 @@ cudaError_t launch_attn(const qsa_dims& d, const void* q, const void* k_cache, c
   a.k_scale = k_scale;
   a.v_scale = v_scale;
   a.sel_row = sel_row;
+  // rows of every KV head of a position stay inside the cache
+  a.row_lim = (int)((long long)d.num_pages * d.n_kv_heads * d.page_size - (long long)(d.n_kv_heads - 1) * d.page_size);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.tickets = tickets;
   a.partials = partials;

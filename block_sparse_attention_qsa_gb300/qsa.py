@@ -33,6 +33,7 @@ EXPORTS = (
     "qsa_workspace_init", "qsa_compress_keys", "qsa_score", "qsa_topk", "qsa_sparse_attn",
     "qsa_decode", "qsa_check_errors", "qsa_sparse_attn_noalloc", "qsa_draft_attn",
     "qsa_compress_keys_paged", "qsa_score_paged", "qsa_decode_paged", "qsa_score_chunk",
+    "qsa_resolve", "qsa_sparse_attn_rows",
 )
 
 MAX_DRAFT_GAP = 64  # QSA_MAX_DRAFT_GAP
@@ -83,6 +84,8 @@ def _load() -> ctypes.CDLL:
         "qsa_score_paged": (I, [D, P, P, P, P, P, P, SZ, P]),
         "qsa_decode_paged": (I, [D, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "qsa_score_chunk": (I, [D, ctypes.c_int32, P, P, P, P, P, SZ, P]),
+        "qsa_resolve": (I, [D, P, P, P, P, P, SZ, P]),
+        "qsa_sparse_attn_rows": (I, [D, P, P, P, P, P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -226,6 +229,34 @@ def sparse_attn(d: Dims, q, k_cache, v_cache, k_scale, v_scale, page_table, sel_
     _check(lib.qsa_sparse_attn(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                _ptr(v_scale), _ptr(page_table), _ptr(sel_pos), _ptr(q_pos), _ptr(out), w, n,
                                _stream(stream)), "qsa_sparse_attn")
+
+
+def resolve(d: Dims, sel_pos, q_pos, page_table, sel_row, ws, stream=None):
+    """Selected positions -> cache rows of KV head 0 (-1 for none or rejected)."""
+    _want(sel_pos, "sel_pos", (d.batch, d.n_q, d.width), torch.int32)
+    _want(q_pos, "q_pos", (d.batch, d.n_q), torch.int32)
+    _want(page_table, "page_table", (d.batch, d.max_pages), torch.int32)
+    _want(sel_row, "sel_row", (d.batch, d.n_q, d.width), torch.int32)
+    w, n = _ws(d, ws)
+    _check(lib.qsa_resolve(ctypes.byref(d), _ptr(sel_pos), _ptr(q_pos), _ptr(page_table), _ptr(sel_row), w, n,
+                           _stream(stream)), "qsa_resolve")
+
+
+def sparse_attn_rows(d: Dims, q, k_cache, v_cache, k_scale, v_scale, sel_row, out, ws, stream=None):
+    """sparse_attn over cache rows written by resolve."""
+    _want(q, "q", (d.batch, d.n_q, d.n_q_heads, d.head_dim), torch.bfloat16)
+    kv_shape = (d.num_pages, d.n_kv_heads, d.page_size, d.head_dim)
+    _want(k_cache, "k_cache", kv_shape, _kv_dtype(d))
+    _want(v_cache, "v_cache", kv_shape, _kv_dtype(d))
+    if d.kv_dtype == KV_FP8_E4M3 or k_scale is not None:
+        _want(k_scale, "k_scale", (d.n_kv_heads,), torch.float32)
+        _want(v_scale, "v_scale", (d.n_kv_heads,), torch.float32)
+    _want(sel_row, "sel_row", (d.batch, d.n_q, d.width), torch.int32)
+    _want(out, "out", (d.batch, d.n_q, d.n_q_heads, d.head_dim), torch.bfloat16)
+    w, n = _ws(d, ws)
+    _check(lib.qsa_sparse_attn_rows(ctypes.byref(d), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                    _ptr(v_scale), _ptr(sel_row), _ptr(out), w, n, _stream(stream)),
+           "qsa_sparse_attn_rows")
 
 
 def sparse_attn_noalloc(d: Dims, q, k_cache, v_cache, k_scale, v_scale, page_table, sel_pos, q_pos, out,

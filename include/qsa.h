@@ -18,8 +18,9 @@
  * Around the step: qsa_compress_keys (the compressed keys themselves),
  * qsa_draft_attn (MTP draft steps reusing a selection), the *_paged entry
  * points (compressed keys kept in the KV cache's pages), qsa_score_chunk
- * (scoring a chunk of many queries per request) and qsa_sparse_attn_noalloc
- * (attention without a caller workspace).
+ * (scoring a chunk of many queries per request), qsa_sparse_attn_noalloc
+ * (attention without a caller workspace), and qsa_resolve /
+ * qsa_sparse_attn_rows (qsa_sparse_attn's two launches, separately).
  *
  * Readings where the pages are silent:
  *   - full blocks of a query at position p: b < (p + 1) / 4; the unfilled
@@ -186,6 +187,24 @@ qsa_status qsa_sparse_attn(const qsa_dims* dims, const void* q, const void* k_ca
                            const void* v_cache, const float* k_scale, const float* v_scale,
                            const int32_t* page_table, const int32_t* sel_pos, const int32_t* q_pos,
                            void* out, void* ws, size_t ws_bytes, void* stream);
+
+/* qsa_sparse_attn in its two launches. qsa_resolve turns the selected
+ * positions into cache rows: sel_row[r][j][i] = the row of position
+ * sel_pos[r][j][i] for KV head 0 in k_cache / v_cache viewed as
+ * [num_pages * n_kv_heads * page_size][128], i.e.
+ * (page_table[r][t / page_size] * n_kv_heads) * page_size + t % page_size
+ * (KV head g adds g * page_size), and -1 where sel_pos is -1 or the position
+ * is rejected (after q_pos[r][j], or its page id outside the cache: reported
+ * as in qsa_sparse_attn). sel_row is [B][n_q][width] int32, caller-owned.
+ * qsa_sparse_attn_rows is the attention of qsa_sparse_attn over such rows
+ * (same output, bit for bit); a row below 0, or one whose last KV head would
+ * lie outside the cache, is skipped without a report. Rows computed once can
+ * serve several attention calls. */
+qsa_status qsa_resolve(const qsa_dims* dims, const int32_t* sel_pos, const int32_t* q_pos,
+                       const int32_t* page_table, int32_t* sel_row, void* ws, size_t ws_bytes, void* stream);
+qsa_status qsa_sparse_attn_rows(const qsa_dims* dims, const void* q, const void* k_cache, const void* v_cache,
+                                const float* k_scale, const float* v_scale, const int32_t* sel_row, void* out,
+                                void* ws, size_t ws_bytes, void* stream);
 
 /* The fused step (bullet 4: "QSA logits -> select -> attention" chained with
  * programmatic dependent launch): qsa_score, qsa_topk and qsa_sparse_attn

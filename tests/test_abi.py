@@ -28,7 +28,7 @@ def _declared():
 
 def test_exports_every_declared_symbol(qsa):
     names = _declared()
-    assert len(names) == 17
+    assert len(names) == 19
     assert set(names) == set(qsa.EXPORTS)
     lib = ctypes.CDLL(qsa.LIB_PATH)
     for n in names:
@@ -91,6 +91,10 @@ def test_workspace_size_and_rejections_need_no_gpu(qsa):
     assert qsa.lib.qsa_topk(ctypes.byref(d), fake, fake, fake, fake, None, n.value, None) == qsa.ERR_WORKSPACE
     assert qsa.lib.qsa_topk(ctypes.byref(d), fake, fake, fake, fake, ctypes.c_void_p((1 << 20) + 8), n.value,
                             None) == qsa.ERR_WORKSPACE
+    # resolve / attention over rows: null pointers
+    assert qsa.lib.qsa_resolve(ctypes.byref(d), fake, fake, None, fake, fake, n.value, None) == qsa.ERR_INVALID_ARG
+    assert qsa.lib.qsa_sparse_attn_rows(ctypes.byref(d), fake, fake, fake, None, None, None, fake, fake, n.value,
+                                        None) == qsa.ERR_INVALID_ARG
     # chunked scoring: chunk length and batch limits
     assert qsa.lib.qsa_score_chunk(ctypes.byref(d), 0, fake, fake, fake, fake, fake, n.value,
                                    None) == qsa.ERR_INVALID_ARG

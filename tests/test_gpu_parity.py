@@ -277,6 +277,49 @@ def test_sparse_attn_parity_on_oracle_selection(qsa, name):
             assert err <= ATOL[spec.kv_dtype], (r, j, err)
 
 
+@pytest.mark.parametrize("name", ["b2-h1-bf16", "b2-p16-fp8"])
+def test_resolve_then_rows_attention_equals_sparse_attn(qsa, name):
+    # qsa_sparse_attn's two launches called one by one: the same rows and the
+    # same output bit for bit; rows outside the cache are skipped like -1
+    spec = SPECS[name]()
+    inp = synth.make_inputs(spec)
+    npi = to_numpy_inputs(inp)
+    npi["kc"] = _kc_oracle(npi, spec)
+    res = O.decode_step(npi, spec.kv_dtype)
+    sel = torch.from_numpy(np.stack([np.stack([res["sel_pos"][(r, j)] for j in range(spec.n_q)])
+                                     for r in range(spec.batch)])).cuda()
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    g = _dev(inp)
+    ref = torch.empty((spec.batch, spec.n_q, 16, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.sparse_attn(d, g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"], g["page_table"], sel,
+                    g["q_pos"], ref, ws)
+    rows = torch.full_like(sel, -7)
+    qsa.resolve(d, sel, g["q_pos"], g["page_table"], rows, ws)
+    out = torch.empty_like(ref)
+    qsa.sparse_attn_rows(d, g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"], rows, out, ws)
+    _check_ok(qsa, ws)
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    # the rows follow the documented formula
+    P, H = spec.page_size, spec.n_kv_heads
+    s_h, r_h, pt = sel.cpu().numpy(), rows.cpu().numpy(), inp["page_table"].numpy()
+    for r in range(spec.batch):
+        for j in range(spec.n_q):
+            t = s_h[r, j]
+            want = np.where(t >= 0, pt[r, np.maximum(t, 0) // P] * H * P + np.maximum(t, 0) % P, -1)
+            assert np.array_equal(r_h[r, j], want), (r, j)
+    # out-of-range rows planted where -1 was: skipped, the output is unchanged
+    bad = rows.clone()
+    lim = d.num_pages * H * P - (H - 1) * P
+    holes = bad < 0
+    bad[holes] = torch.tensor([lim, lim + 5, 2 ** 31 - 1, -2], dtype=torch.int32, device="cuda").repeat(
+        int(holes.sum().item()) // 4 + 1)[: int(holes.sum().item())]
+    out2 = torch.empty_like(ref)
+    qsa.sparse_attn_rows(d, g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"], bad, out2, ws)
+    _check_ok(qsa, ws)
+    assert torch.equal(out2.view(torch.int16), ref.view(torch.int16))
+
+
 def test_sparse_attn_with_holes_and_single_positions(qsa):
     spec = small_spec([4000, 130], n_q=2, seed=21)
     inp = synth.make_inputs(spec)
