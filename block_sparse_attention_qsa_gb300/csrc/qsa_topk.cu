@@ -22,7 +22,9 @@
 // selected blocks ascending, the lowest-index ties first, and all threads
 // write the outputs from that list with coalesced stores. Longer rows run the
 // radix passes over the whole row (keys cached in shared memory when they
-// fit) and list the selection in index order tile by tile. The request's
+// fit, else read with several loads in flight), mark the selected and tied
+// blocks in two shared bitmaps with warp ballots, and list them with one
+// block scan over contiguous bitmap words per thread. The request's
 // page table is staged in shared memory (before waiting on the score kernel,
 // for a CTA's first row) so the cache rows written inside qsa_decode need no
 // dependent global loads.
@@ -346,6 +348,19 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
       // ---- long rows: radix passes over the whole row ----
       const bool in_smem = n <= key_cap;  // keys cached in shared memory
       uint32_t* keys = body;
+      // f(i, valid, key) for the blocks [c0, c0 + cn), on all lanes of a warp
+      // together (a warp's lanes take 32 consecutive blocks); global scores are
+      // read with kBatch loads in flight
+      auto each_key = [&](int c0, int cn, auto&& f) {
+        if (in_smem) {
+          for (int wb = tid & ~31; wb < cn; wb += kThreads) {  // warp-uniform
+            const int i = wb + lane;
+            f(i, i < cn, i < cn ? keys[c0 + i] : 0u);
+          }
+        } else {
+          for_each_score(srow + c0, cn, f);
+        }
+      };
       for_each_score(srow, n, [&](int i, bool ok, uint32_t k) {
         if (in_smem && ok) keys[i] = k;
         hist_add(hist, ok, k >> 21, lane);
@@ -357,56 +372,84 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
       need -= (uint32_t)res[1];
       for (int i = tid; i < 2048; i += kThreads) hist[i] = 0;
       __syncthreads();
-      auto key_at = [&](int i) { return in_smem ? keys[i] : order_key(srow[i]); };
-      for (int i = tid; i < n; i += kThreads) {
-        const uint32_t k = key_at(i);
-        if ((k >> 21) == d1) atomicAdd(&hist[(k >> 10) & 2047u], 1u);
-      }
+      each_key(0, n, [&](int, bool ok, uint32_t k) {
+        if (ok && (k >> 21) == d1) atomicAdd(&hist[(k >> 10) & 2047u], 1u);
+      });
       __syncthreads();
       find_bin<2048>(hist, need, wsum, res);
-      const uint32_t prefix = (d1 << 11) | (uint32_t)res[0];
+      const uint32_t d2 = (uint32_t)res[0];
       need -= (uint32_t)res[1];
-      for (int i = tid; i < 1024; i += kThreads) hist[i] = 0;
-      __syncthreads();
-      for (int i = tid; i < n; i += kThreads) {
-        const uint32_t k = key_at(i);
-        if ((k >> 10) == prefix) atomicAdd(&hist[k & 1023u], 1u);
-      }
-      __syncthreads();
-      find_bin<1024>(hist, need, wsum, res);
-      const uint32_t T = (prefix << 10) | (uint32_t)res[0];
-      need -= (uint32_t)res[1];
-
-      // ordered listing: keys > T, then the first `need` keys == T
-      uint32_t n_sel = 0, n_tie = 0;
-      int buf = 0;
-      for (int base = 0; base < n; base += kThreads) {
-        const int i = base + tid;
-        const uint32_t k = (i < n) ? key_at(i) : 0u;
-        const bool gt = (i < n) && k > T;
-        const bool eq = (i < n) && k == T;
-        const uint32_t gtm = __ballot_sync(kFull, gt);
-        const uint32_t eqm = __ballot_sync(kFull, eq);
-        uint32_t* wc = wsum + 32 * buf;
-        if (lane == 0) wc[warp] = ((uint32_t)__popc(eqm) << 16) | (uint32_t)__popc(gtm);
+      const uint32_t prefix = (d1 << 11) | d2;
+      // when digit 2's bin is taken whole, no third digit is needed
+      const bool whole = hist[d2] == need;
+      uint32_t T = prefix << 10;
+      __syncthreads();  // every thread has read hist[d2]
+      if (!whole) {
+        for (int i = tid; i < 1024; i += kThreads) hist[i] = 0;
         __syncthreads();
-        const uint32_t c = wc[lane];
-        const uint32_t incl = warp_incl_scan(c, lane);
-        const uint32_t excl_w = __shfl_sync(kFull, incl - c, warp);
-        const uint32_t tot = __shfl_sync(kFull, incl, 31);
-        const uint32_t E_w = excl_w >> 16, G_w = excl_w & 0xffffu;
-        const uint32_t E_t = tot >> 16, G_t = tot & 0xffffu;
-        const uint32_t rem_tile = need > n_tie ? need - n_tie : 0u;
-        const uint32_t taken_before = min(rem_tile, E_w);
-        const uint32_t rem_w = rem_tile > E_w ? rem_tile - E_w : 0u;
-        const uint32_t my_eq = (uint32_t)__popc(eqm & lt_mask);
-        if (gt || (eq && my_eq < rem_w)) {
-          const uint32_t slot = n_sel + G_w + taken_before + (uint32_t)__popc(gtm & lt_mask) + min(my_eq, rem_w);
-          if (slot < (uint32_t)kTopK) blk[slot] = i;
+        each_key(0, n, [&](int, bool ok, uint32_t k) {
+          if (ok && (k >> 10) == prefix) atomicAdd(&hist[k & 1023u], 1u);
+        });
+        __syncthreads();
+        find_bin<1024>(hist, need, wsum, res);
+        T |= (uint32_t)res[0];
+        need -= (uint32_t)res[1];  // blocks equal to T still to take, >= 1
+      } else {
+        need = 0;
+      }
+
+      // ordered listing, 65,536 blocks at a time: one ballot pass marks the
+      // selected blocks (key >= cut) and the tied ones (key == T, unless digit
+      // 2's bin is taken whole) in two shared bitmaps (the histograms' space);
+      // then each thread owns a contiguous run of bitmap words, and one block
+      // scan of the per-thread counts gives every pick its slot: ascending
+      // blocks, the lowest-index ties first
+      uint32_t* sel_bits = hist2;  // [2048]
+      uint32_t* tie_bits = hist;   // [2048]
+      const uint32_t cut = whole ? T : T + 1u;  // T < 2^32 - 1 here
+      uint32_t sel_done = 0, tie_done = 0;  // counts in the chunks before (the same in every thread)
+      for (int c0 = 0; c0 < n; c0 += 65536) {
+        const int cn = min(65536, n - c0);
+        const int nw = (cn + 31) >> 5;
+        __syncthreads();  // the histograms / previous chunk's bitmaps are no longer read
+        each_key(c0, cn, [&](int i, bool ok, uint32_t k) {
+          const uint32_t sb = __ballot_sync(kFull, ok && k >= cut);
+          const uint32_t tb = __ballot_sync(kFull, ok && !whole && k == T);
+          if (lane == 0) {
+            sel_bits[i >> 5] = sb;
+            tie_bits[i >> 5] = tb;
+          }
+        });
+        __syncthreads();
+        const int wpt = (nw + kThreads - 1) / kThreads;  // bitmap words per thread
+        const int w0 = min(nw, tid * wpt), w1 = min(nw, w0 + wpt);
+        uint32_t cs = 0, ce = 0;
+        for (int w = w0; w < w1; ++w) {
+          cs += (uint32_t)__popc(sel_bits[w]);
+          ce += (uint32_t)__popc(tie_bits[w]);
         }
-        n_sel += G_t + min(rem_tile, E_t);
-        n_tie += E_t;
-        buf ^= 1;
+        // selected blocks number at most kTopK (< 2^11); ties at most 65,536
+        uint32_t total;
+        const uint32_t excl = block_excl_scan((ce << 11) | cs, wsum, &total);
+        const uint32_t e_before = tie_done + (excl >> 11), s_before = sel_done + (excl & 2047u);
+        uint32_t take = need > e_before ? min(need - e_before, ce) : 0u;
+        uint32_t slot = s_before + min(e_before, need);
+        for (int w = w0; w < w1; ++w) {
+          uint32_t tb = tie_bits[w], keep = 0;
+          for (; take > 0 && tb; --take) {  // the lowest ties are taken
+            keep |= tb & (0u - tb);
+            tb &= tb - 1u;
+          }
+          uint32_t pick = sel_bits[w] | keep;
+          while (pick) {
+            const int bit = __ffs(pick) - 1;
+            if (slot < (uint32_t)kTopK) blk[slot] = c0 + 32 * w + bit;  // exactly kTopK; the bound is a guard
+            ++slot;
+            pick &= pick - 1u;
+          }
+        }
+        sel_done += total & 2047u;
+        tie_done += total >> 11;
       }
     }
     __syncthreads();  // the selection list is complete
