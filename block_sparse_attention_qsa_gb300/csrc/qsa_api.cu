@@ -9,15 +9,14 @@
 namespace qsa {
 
 int device_sm_count() {
-  static int cache[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  if (dev < 64 && cache[dev] > 0) return cache[dev];
-  int n = 0;
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  if (n < 1) n = 1;
-  if (dev < 64) cache[dev] = n;
-  return n;
+  static DeviceSlots sms;
+  const int n = sms.get([] {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return v;
+  });
+  return n > 0 ? n : 1;
 }
 
 WsLayout ws_layout(const qsa_dims& d, int num_sms) {
@@ -145,6 +144,7 @@ qsa_status qsa_compress_keys(const qsa_dims* dims, const void* idx_keys, const i
                              void* stream) {
   qsa_status st = check_dims(dims);
   if (st != QSA_OK) return st;
+  if (dims->batch > 65535) return QSA_ERR_UNSUPPORTED;  // one grid row (y) per request
   if (!idx_keys || !q_pos || !kc) return QSA_ERR_INVALID_ARG;
   if (!aligned16(idx_keys) || !aligned16(kc)) return QSA_ERR_INVALID_ARG;
   if ((st = check_ws(dims, ws, ws_bytes, nullptr)) != QSA_OK) return st;
@@ -159,6 +159,7 @@ qsa_status qsa_compress_keys_paged(const qsa_dims* dims, const void* idx_keys, c
                                    void* ws, size_t ws_bytes, void* stream) {
   qsa_status st = check_dims(dims);
   if (st != QSA_OK) return st;
+  if (dims->batch > 65535) return QSA_ERR_UNSUPPORTED;  // one grid row (y) per request
   if (!idx_keys || !q_pos || !page_table || !kc_cache) return QSA_ERR_INVALID_ARG;
   if (!aligned16(idx_keys) || !aligned16(kc_cache)) return QSA_ERR_INVALID_ARG;
   if ((st = check_ws(dims, ws, ws_bytes, nullptr)) != QSA_OK) return st;
@@ -172,6 +173,7 @@ qsa_status qsa_score_paged(const qsa_dims* dims, const void* q_idx, const void* 
                            size_t ws_bytes, void* stream) {
   qsa_status st = check_dims(dims);
   if (st != QSA_OK) return st;
+  if (dims->batch > QSA_MAX_SCORE_BATCH) return QSA_ERR_UNSUPPORTED;  // per-request tables in shared memory
   if (!q_idx || !kc_cache || !page_table || !q_pos || !scores) return QSA_ERR_INVALID_ARG;
   if (!aligned16(q_idx) || !aligned16(kc_cache)) return QSA_ERR_INVALID_ARG;
   if ((st = check_ws(dims, ws, ws_bytes, nullptr)) != QSA_OK) return st;
@@ -184,6 +186,7 @@ qsa_status qsa_score(const qsa_dims* dims, const void* q_idx, const void* kc, co
                      float* scores, void* ws, size_t ws_bytes, void* stream) {
   qsa_status st = check_dims(dims);
   if (st != QSA_OK) return st;
+  if (dims->batch > QSA_MAX_SCORE_BATCH) return QSA_ERR_UNSUPPORTED;  // per-request tables in shared memory
   if (!q_idx || !kc || !q_pos || !scores) return QSA_ERR_INVALID_ARG;
   if (!aligned16(q_idx) || !aligned16(kc)) return QSA_ERR_INVALID_ARG;
   if ((st = check_ws(dims, ws, ws_bytes, nullptr)) != QSA_OK) return st;
@@ -277,6 +280,7 @@ qsa_status decode_impl(const qsa_dims* dims, const void* q_idx, const void* kc, 
                        int32_t* sel_pos, void* out, void* ws, size_t ws_bytes, void* stream, bool kc_paged) {
   qsa_status st = check_dims(dims);
   if (st != QSA_OK) return st;
+  if (dims->batch > QSA_MAX_SCORE_BATCH) return QSA_ERR_UNSUPPORTED;  // per-request tables in shared memory
   if (!q_idx || !kc || !q || !k_cache || !v_cache || !page_table || !q_pos || !out)
     return QSA_ERR_INVALID_ARG;
   if (dims->kv_dtype == QSA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return QSA_ERR_INVALID_ARG;

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <utility>
 
 #include "qsa.h"
@@ -59,6 +60,43 @@ AttnPlan attn_plan(const qsa_dims& d, int num_sms);
 WsLayout ws_layout(const qsa_dims& d, int num_sms);
 
 int device_sm_count();
+
+// Host-side per-device state of a launcher (SM count, occupancy, the dynamic
+// shared-memory limit set on a kernel), safe to use from several host threads.
+class DeviceSlots {
+ public:
+  static constexpr int kMaxDevices = 64;
+  // the current device's value, computed by init() on first use; a result
+  // <= 0 is returned but not kept, so a failed query is retried next time
+  template <typename F>
+  int get(F&& init) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return init();
+    std::lock_guard<std::mutex> lock(mu_);
+    if (v_[dev] <= 0) v_[dev] = init();
+    return v_[dev];
+  }
+  // raises kern's dynamic shared-memory limit on the current device to at
+  // least `bytes` (never lowers it, so concurrent callers cannot undo each other)
+  template <typename K>
+  cudaError_t raise_smem(K kern, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices)
+      return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    std::lock_guard<std::mutex> lock(mu_);
+    if ((size_t)v_[dev] >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) v_[dev] = (int)bytes;
+    return e;
+  }
+
+ private:
+  std::mutex mu_;
+  int v_[kMaxDevices] = {};
+};
 
 // ---------------------------------------------------------------------------
 // device helpers

@@ -186,15 +186,8 @@ cudaError_t launch_score_chunk(const qsa_dims& d, int n_chunk, const __nv_bfloat
   const size_t smem = (size_t)(d.n_idx_heads > 1 ? 2 : 1) * kStageElems * sizeof(__nv_bfloat16);
   static_assert((size_t)kBN * kOutLd * sizeof(float) <= (size_t)kStageElems * sizeof(__nv_bfloat16),
                 "output tile larger than a stage buffer");
-  static size_t set_bytes[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 64 || set_bytes[dev] < smem) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(score_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) set_bytes[dev] = smem;
-  }
+  static DeviceSlots smem_slots;
+  if (const cudaError_t e = smem_slots.raise_smem(score_chunk_kernel, smem); e != cudaSuccess) return e;
   const dim3 grid((d.max_blocks + kBM - 1) / kBM, (n_chunk + kBN - 1) / kBN, d.batch);
   return launch_k(score_chunk_kernel, grid, dim3(kPThreads), smem, s, false, q_idx, kc, q_pos, scores, err, n_chunk,
                   d.n_idx_heads, d.max_blocks);

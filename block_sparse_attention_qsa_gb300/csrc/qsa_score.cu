@@ -330,16 +330,15 @@ cudaError_t launch_score_h(const qsa_dims& d, const __nv_bfloat16* q_idx, const 
                            bool pdl, const KcPages& kp) {
   auto kern = score_kernel<H, PAGED>;
   const size_t smem = (size_t)(2 * d.batch + 1) * sizeof(int);
-  static int occ_cache[64] = {0};  // one per instantiation
-  int dev = 0;
-  cudaGetDevice(&dev);
-  int occ = dev < 64 ? occ_cache[dev] : 0;
-  if (occ == 0) {
-    if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 256, smem);
-    if (occ < 1) occ = 1;
-    if (dev < 64 && smem <= 48 * 1024) occ_cache[dev] = occ;
-  }
+  static DeviceSlots occ_slots, smem_slots;  // one pair per instantiation
+  const cudaError_t e = smem_slots.raise_smem(kern, smem);
+  if (e != cudaSuccess) return e;
+  // resident CTAs per SM: bound by registers (the per-request tables are small)
+  int occ = occ_slots.get([&] {
+    int o = 0;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, 256, 0) == cudaSuccess ? o : 0;
+  });
+  if (occ < 1) occ = 1;
   // upper bound of the work, in 16-block units, to avoid launching idle warps
   const long long units_ub = (long long)d.batch * ((d.max_blocks + 15) / 16);
   long long warps = (long long)device_sm_count() * occ * 8;

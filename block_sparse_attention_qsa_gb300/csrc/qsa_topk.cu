@@ -716,14 +716,8 @@ cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q
   const int key_cap = mb > kFastCap ? (mb < kKeyCap ? mb : kKeyCap) : 0;
   const size_t body = (size_t)key_cap;  // the register path needs no body
   const size_t smem = (kHdrWords + body) * sizeof(uint32_t);
-  static size_t set_bytes[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 64 || set_bytes[dev] < smem) {
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) set_bytes[dev] = smem;
-  }
+  static DeviceSlots smem_slots;
+  if (const cudaError_t e = smem_slots.raise_smem(topk_kernel, smem); e != cudaSuccess) return e;
   int grid = rows < device_sm_count() ? rows : device_sm_count();
   if (grid < 1) grid = 1;
   RowOut ro;

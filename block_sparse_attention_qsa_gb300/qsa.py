@@ -38,6 +38,7 @@ EXPORTS = (
 
 MAX_DRAFT_GAP = 64  # QSA_MAX_DRAFT_GAP
 MAX_CHUNK = 65536  # QSA_MAX_CHUNK
+MAX_SCORE_BATCH = 16384  # QSA_MAX_SCORE_BATCH
 
 
 class QSAError(RuntimeError):

@@ -93,6 +93,11 @@ extern "C" {
  * reuses (qsa_draft_attn). */
 #define QSA_MAX_DRAFT_GAP 64
 
+/* Most requests in one qsa_score / qsa_score_paged / qsa_decode /
+ * qsa_decode_paged call (the scoring kernel keeps two small per-request tables
+ * in shared memory); larger batches return QSA_ERR_UNSUPPORTED. */
+#define QSA_MAX_SCORE_BATCH 16384
+
 /* Most queries per request in one qsa_score_chunk call. */
 #define QSA_MAX_CHUNK 65536
 
@@ -152,7 +157,8 @@ qsa_status qsa_workspace_init(void* ws, size_t ws_bytes, void* stream);
  * reading: FP32 mean of the 4 keys, summed in token order, rounded to BF16).
  * For request r, writes kc[r][b] for block_lo[r] <= b < (P_r + 1) / 4 where
  * P_r = max_j q_pos[r][j]; block_lo may be NULL (= 0 for every request), so
- * an engine can refresh only the blocks its newest tokens completed. */
+ * an engine can refresh only the blocks its newest tokens completed. At most
+ * 65,535 requests per call (also for qsa_compress_keys_paged). */
 qsa_status qsa_compress_keys(const qsa_dims* dims, const void* idx_keys, const int32_t* q_pos,
                              const int32_t* block_lo, void* kc, void* ws, size_t ws_bytes,
                              void* stream);

@@ -41,6 +41,8 @@ def test_draft_gap_matches_the_header(qsa):
     assert m and int(m.group(1)) == qsa.MAX_DRAFT_GAP
     m = re.search(r"#define QSA_MAX_CHUNK (\d+)", txt)
     assert m and int(m.group(1)) == qsa.MAX_CHUNK
+    m = re.search(r"#define QSA_MAX_SCORE_BATCH (\d+)", txt)
+    assert m and int(m.group(1)) == qsa.MAX_SCORE_BATCH
 
 
 def test_abi_version_and_status_strings(qsa):
@@ -100,6 +102,9 @@ def test_workspace_size_and_rejections_need_no_gpu(qsa):
                                    None) == qsa.ERR_INVALID_ARG
     assert qsa.lib.qsa_score_chunk(ctypes.byref(d), qsa.MAX_CHUNK + 1, fake, fake, fake, fake, fake, n.value,
                                    None) == qsa.ERR_INVALID_ARG
+    # scoring: batch limit
+    huge = qsa.make_dims(qsa.MAX_SCORE_BATCH + 1, 1, 4, 1, 1)
+    assert qsa.lib.qsa_score(ctypes.byref(huge), fake, fake, fake, fake, fake, 1 << 40, None) == qsa.ERR_UNSUPPORTED
     big = qsa.make_dims(65536, 1, 4, 1, 1)
     assert qsa.lib.qsa_score_chunk(ctypes.byref(big), 1, fake, fake, fake, fake, fake, 1 << 40,
                                    None) == qsa.ERR_UNSUPPORTED
