@@ -155,6 +155,29 @@ def test_score_full_size_every_row(qsa, config, batch, ctx):
             assert np.all(np.isnan(got[r, j, nb:]))
 
 
+def test_score_batch_with_tables_beyond_48kb(qsa):
+    # 7,000 short requests: the scoring kernel's per-request tables need more
+    # than the default 48 KB of shared memory, raised by the launcher on use
+    B, n_q, mb = 7000, 2, 12
+    d = qsa.make_dims(B, n_q, mb, 1, 1)
+    ws = qsa.make_workspace(d)
+    q_idx = synth.normal_bf16((B, n_q, 1, 128), 501, "cuda")
+    kc = synth.normal_bf16((B, mb, 1, 128), 502, "cuda")
+    pos = [[(7 * r) % 48, (7 * r) % 48 + 1] for r in range(B)]
+    q_pos = torch.tensor(pos, dtype=torch.int32, device="cuda")
+    scores = torch.full((B, n_q, mb), float("nan"), device="cuda")
+    qsa.score(d, q_idx, kc, q_pos, scores, ws)
+    _check_ok(qsa, ws)
+    qb, kb, got = bits(q_idx), bits(kc), scores.cpu().numpy()
+    for r in (0, 1, 2, 3999, 6997, 6998, 6999):
+        for j in range(n_q):
+            ref = O.score_row(qb[r, j], kb[r], pos[r][j])
+            nb = ref.shape[0]
+            err = np.abs(got[r, j, :nb].astype(np.float64) - ref) / np.maximum(np.abs(ref), 1.0)
+            assert nb == 0 or err.max() <= SCORE_RTOL, (r, j)
+            assert np.all(np.isnan(got[r, j, nb:]))
+
+
 def _score_rows(kind, n, seed):
     rng = np.random.default_rng(seed)
     if kind == "normal":
