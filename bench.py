@@ -52,7 +52,7 @@ def parse_args():
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--batch", type=int, default=None)
     ap.add_argument("--ctx", type=int, default=None)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="seconds of oracle work in the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-flush", action="store_true", help="warm-L2 numbers (reported as such)")
     ap.add_argument("--step-only", action="store_true",
