@@ -731,10 +731,13 @@ cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q
   ro.n_kv = d.n_kv_heads;
   // Long rows (beyond the register path) and few of them: a cluster of C
   // CTAs per row, the largest C with every CTA on its own SM, when each CTA's
-  // share of the longest row fits KPT <= 32 keys per thread. (Measured: for
-  // rows the register path holds, the cluster's extra barriers and reductions
-  // cost more than splitting the row saves; a batch-1 262,144-token row takes
-  // the step from 121.6 us to 51.3 us.)
+  // share of the longest row fits KPT <= 32 keys per thread (a batch-1
+  // 262,144-token row takes the step from 121.6 us to 51.3 us). Rows the
+  // register path holds are split in two only when the rows are very few:
+  // measured at 15K blocks, a pair of CTAs per row takes a batch-1 step from
+  // 33.1 to 31.2 us and batch 4 from 37.6 to 36.6 us, makes no difference
+  // from 32 rows on, and 4 or 8 CTAs per row gain nothing more (their
+  // barriers and reductions cost what the split saves).
   const int sms = device_sm_count();
   int C = 1;
   for (int c = kMaxCluster; c >= 2; c >>= 1)
@@ -742,7 +745,8 @@ cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q
       C = c;
       break;
     }
-  if (C > 1 && mb > kFastCap) {
+  if (mb <= kFastCap) C = (mb > 4096 && (long long)rows * 8 <= sms) ? 2 : 1;
+  if (C > 1) {
     const int per_thread = ((mb + C - 1) / C + kThreads - 1) / kThreads;
     cudaError_t e = cudaErrorNotSupported;
     if (per_thread <= 4)
