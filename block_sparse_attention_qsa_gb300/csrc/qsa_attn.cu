@@ -522,13 +522,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
       for (int h = 0; h < 8; ++h) part[16 + h * kDim + tid] = o[h];
       const long long uw0 = (long long)u * a.tiles;
       const int c_first = cta_of_tile(a, uw0), n_piece = cta_of_tile(a, uw0 + a.tiles - 1) - c_first + 1;
-      __threadfence();
+      // the barrier orders every thread's stores of the piece before thread 0's
+      // fence, which makes them visible before the ticket is taken
       __syncthreads();
-      if (tid == 0) s_last = (atomicAdd(&a.tickets[u], 1) == n_piece - 1);
+      if (tid == 0) {
+        __threadfence();
+        s_last = (atomicAdd(&a.tickets[u], 1) == n_piece - 1);
+      }
       __syncthreads();
       if (s_last) {
         __threadfence();
-        // every piece's (max, sum) at once, then the accumulators kMergeBatch pieces at a time
+        // every piece's (max, sum) at once, with the first kMergeBatch pieces'
+        // accumulators already on their way; then the rest kMergeBatch at a time
         float* pm = wacc;                        // [n_piece][8] (the merge buffer is free now)
         float* pl = wacc + n_piece * kGroup;     // [n_piece][8]
         int* ps = reinterpret_cast<int*>(wacc + 2 * n_piece * kGroup);  // [n_piece] slots
@@ -537,6 +542,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
           ps[k] = 2 * cc + (tile_begin(a, cc) >= uw0 ? 0 : 1);
         }
         __syncthreads();
+        float x[kMergeBatch][8];  // 32 loads in flight per thread
+        auto load_batch = [&](int k0) {
+#pragma unroll
+          for (int kk = 0; kk < kMergeBatch; ++kk) {
+            const bool in = k0 + kk < n_piece;
+            const float* pp = a.partials + (size_t)(in ? ps[k0 + kk] : 0) * kPartFloats + 2 * kGroup + tid;
+#pragma unroll
+            for (int h = 0; h < 8; ++h) x[kk][h] = in ? __ldcg(pp + h * kDim) : 0.f;
+          }
+        };
+        load_batch(0);
         for (int i = tid; i < n_piece * kGroup; i += kThreads) {
           const float* pp = a.partials + (size_t)ps[i >> 3] * kPartFloats;
           pm[i] = __ldcg(pp + (i & 7));
@@ -556,14 +572,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
 #pragma unroll
         for (int h = 0; h < 8; ++h) o[h] = 0.f;
         for (int k0 = 0; k0 < n_piece; k0 += kMergeBatch) {
-          float x[kMergeBatch][8];  // 32 loads in flight per thread
-#pragma unroll
-          for (int kk = 0; kk < kMergeBatch; ++kk) {
-            const bool in = k0 + kk < n_piece;
-            const float* pp = a.partials + (size_t)(in ? ps[k0 + kk] : 0) * kPartFloats + 2 * kGroup + tid;
-#pragma unroll
-            for (int h = 0; h < 8; ++h) x[kk][h] = in ? __ldcg(pp + h * kDim) : 0.f;
-          }
+          if (k0 > 0) load_batch(k0);
 #pragma unroll
           for (int kk = 0; kk < kMergeBatch; ++kk) {
             if (k0 + kk >= n_piece) break;
