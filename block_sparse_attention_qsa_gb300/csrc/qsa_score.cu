@@ -218,18 +218,12 @@ __global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(cons
 #pragma unroll
       for (int s = 0; s < STEPS; ++s) qf[s] = (g < n_q) ? qrow[s * 4 + c] : make_uint4(0, 0, 0, 0);
     }
-    // this lane stores queries 2c, 2c+1 (lanes with c < 2); needed only at the stores
-    int nb0 = 0, nb1 = 0;
-    if (c < 2) {
-      if (2 * c < n_q) {
-        const int p = q_pos[r * n_q + 2 * c];
-        nb0 = (p >= 0 && n_full_of(p) <= max_blocks) ? n_full_of(p) : 0;
-      }
-      if (2 * c + 1 < n_q) {
-        const int p = q_pos[r * n_q + 2 * c + 1];
-        nb1 = (p >= 0 && n_full_of(p) <= max_blocks) ? n_full_of(p) : 0;
-      }
-    }
+    // this lane stores queries 2c, 2c+1 (lanes with c < 2): their positions are
+    // loaded here and turned into block bounds only at the first store, so the
+    // key loads below do not wait for them
+    const int p0 = (c < 2 && 2 * c < n_q) ? q_pos[r * n_q + 2 * c] : -1;
+    const int p1 = (c < 2 && 2 * c + 1 < n_q) ? q_pos[r * n_q + 2 * c + 1] : -1;
+    auto bound = [&](int p) { return (p >= 0 && n_full_of(p) <= max_blocks) ? n_full_of(p) : 0; };
     const uint4* kc_r = kc + (size_t)r * max_blocks * CPB;
     float* sc_r = scores + (size_t)r * n_q * max_blocks;
 
@@ -296,6 +290,11 @@ __global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(cons
         }
         const int b = (u + k - u0) * 16 + g;
         if (c < 2 && u + k < seg_end) {
+          // read here, after the key loads (a volatile move is not hoisted out of the loop)
+          int q0, q1;
+          asm volatile("mov.b32 %0, %1;" : "=r"(q0) : "r"(p0));
+          asm volatile("mov.b32 %0, %1;" : "=r"(q1) : "r"(p1));
+          const int nb0 = bound(q0), nb1 = bound(q1);
           float* s0 = sc_r + (size_t)(2 * c) * max_blocks;
           float* s1 = s0 + max_blocks;
           if (b < nb0) s0[b] = acc[0];
