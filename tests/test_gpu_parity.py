@@ -477,6 +477,16 @@ def test_decode_long_context_262k_row_over_shared_memory(qsa):
     assert skipped <= 1
 
 
+def test_decode_long_context_batch8_cluster_rows_sampled(qsa):
+    # 8 requests x 4 queries of 32,769 blocks: rows longer than the register
+    # path, few enough for a cluster of four CTAs per row (inputs drawn on the
+    # device; the oracle sees the same tensors)
+    spec = synth.spec_for(4, batch=8, ctx=131072)
+    g = synth.make_inputs(spec, device="cuda")
+    skipped, n = _decode_and_compare(qsa, spec, rows=[(0, 0), (3, 2), (7, 3)], gpu_inputs=g)
+    assert skipped <= 1
+
+
 # --------------------------------------------------------------------------
 # invariances and errors
 # --------------------------------------------------------------------------
