@@ -487,6 +487,41 @@ def test_decode_long_context_batch8_cluster_rows_sampled(qsa):
     assert skipped <= 1
 
 
+def test_decode_replayed_as_a_cuda_graph_matches_direct_calls(qsa):
+    # the launch the benchmark times: the fused step captured once as a CUDA
+    # graph (kernels and programmatic dependencies) and replayed, at full size;
+    # its outputs must equal those of direct calls bit for bit, replay after replay
+    spec = synth.spec_for(2)
+    g = synth.make_inputs(spec, device="cuda")
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    kc = torch.zeros((spec.batch, spec.max_blocks(), 1, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.compress_keys(d, g["idx_keys"], g["q_pos"], kc, ws)
+    out = torch.empty((spec.batch, spec.n_q, 16, 128), dtype=torch.bfloat16, device="cuda")
+
+    def step():
+        qsa.decode(d, g["q_idx"], kc, g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"],
+                   g["page_table"], g["q_pos"], out, ws)
+
+    step()
+    torch.cuda.synchronize()
+    direct = out.view(torch.int16).clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(3):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), direct)
+    _check_ok(qsa, ws)
+
+
 # --------------------------------------------------------------------------
 # invariances and errors
 # --------------------------------------------------------------------------
