@@ -229,7 +229,7 @@ qsa_status qsa_sparse_attn(const qsa_dims* dims, const void* q, const void* k_ca
   if (!q || !k_cache || !v_cache || !page_table || !sel_pos || !q_pos || !out)
     return QSA_ERR_INVALID_ARG;
   if (dims->kv_dtype == QSA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return QSA_ERR_INVALID_ARG;
-  if (!aligned16(k_cache) || !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(q) & 3u))
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q))
     return QSA_ERR_INVALID_ARG;
   WsLayout w;
   if ((st = check_ws(dims, ws, ws_bytes, &w)) != QSA_OK) return st;
@@ -259,7 +259,7 @@ qsa_status qsa_sparse_attn_rows(const qsa_dims* dims, const void* q, const void*
   if (st != QSA_OK) return st;
   if (!q || !k_cache || !v_cache || !sel_row || !out) return QSA_ERR_INVALID_ARG;
   if (dims->kv_dtype == QSA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return QSA_ERR_INVALID_ARG;
-  if (!aligned16(k_cache) || !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(q) & 3u))
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q))
     return QSA_ERR_INVALID_ARG;
   WsLayout w;
   if ((st = check_ws(dims, ws, ws_bytes, &w)) != QSA_OK) return st;
@@ -285,7 +285,7 @@ qsa_status decode_impl(const qsa_dims* dims, const void* q_idx, const void* kc, 
     return QSA_ERR_INVALID_ARG;
   if (dims->kv_dtype == QSA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return QSA_ERR_INVALID_ARG;
   if (!aligned16(q_idx) || !aligned16(kc) || !aligned16(k_cache) || !aligned16(v_cache) ||
-      (reinterpret_cast<uintptr_t>(q) & 3u))
+      !aligned16(q))
     return QSA_ERR_INVALID_ARG;
   WsLayout w;
   if ((st = check_ws(dims, ws, ws_bytes, &w)) != QSA_OK) return st;
@@ -337,7 +337,7 @@ qsa_status qsa_draft_attn(const qsa_dims* dims, const void* q, const void* k_cac
     return QSA_ERR_INVALID_ARG;
   if (n_sel < 1 || n_sel > kMaxNq) return QSA_ERR_INVALID_ARG;
   if (dims->kv_dtype == QSA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return QSA_ERR_INVALID_ARG;
-  if (!aligned16(k_cache) || !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(q) & 3u))
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q))
     return QSA_ERR_INVALID_ARG;
   WsLayout w;
   if ((st = check_ws(dims, ws, ws_bytes, &w)) != QSA_OK) return st;

@@ -56,7 +56,7 @@ extern "C" qsa_status qsa_sparse_attn_noalloc(const qsa_dims* dims, const void* 
   if (!q || !k_cache || !v_cache || !page_table || !sel_pos || !q_pos || !out) return QSA_ERR_INVALID_ARG;
   if (dims->kv_dtype == QSA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return QSA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(k_cache) & 15u) || (reinterpret_cast<uintptr_t>(v_cache) & 15u) ||
-      (reinterpret_cast<uintptr_t>(q) & 3u))
+      (reinterpret_cast<uintptr_t>(q) & 15u))
     return QSA_ERR_INVALID_ARG;
 
   // The usual plan, with fewer CTAs (so fewer partials) if it would not fit.

@@ -66,6 +66,11 @@
  * output; a bad selected position or page is left out of the softmax);
  * qsa_check_errors() reports them. No call aborts or throws.
  *
+ * Alignment: idx_keys, q_idx, kc (or kc_cache), q, k_cache and v_cache are read with
+ * 16-byte vector loads or copies and must be 16-byte aligned; the other
+ * arrays need the alignment of their element type. A misaligned pointer
+ * returns QSA_ERR_INVALID_ARG before anything is launched.
+ *
  * Workspace: every entry point takes `ws`, a caller-owned device buffer of at
  * least qsa_workspace_size() bytes, 256-byte aligned, zero-filled once before
  * its first use (qsa_workspace_init). The kernels leave it in a state ready

@@ -93,6 +93,12 @@ def test_workspace_size_and_rejections_need_no_gpu(qsa):
     assert qsa.lib.qsa_topk(ctypes.byref(d), fake, fake, fake, fake, None, n.value, None) == qsa.ERR_WORKSPACE
     assert qsa.lib.qsa_topk(ctypes.byref(d), fake, fake, fake, fake, ctypes.c_void_p((1 << 20) + 8), n.value,
                             None) == qsa.ERR_WORKSPACE
+    # the attention query is copied 16 bytes at a time: a 4-byte-aligned one is refused
+    q4 = ctypes.c_void_p((1 << 20) + 4)
+    assert qsa.lib.qsa_sparse_attn(ctypes.byref(d), q4, fake, fake, None, None, fake, fake, fake, fake, fake,
+                                   n.value, None) == qsa.ERR_INVALID_ARG
+    assert qsa.lib.qsa_sparse_attn_rows(ctypes.byref(d), q4, fake, fake, None, None, fake, fake, fake, n.value,
+                                        None) == qsa.ERR_INVALID_ARG
     # resolve / attention over rows: null pointers
     assert qsa.lib.qsa_resolve(ctypes.byref(d), fake, fake, None, fake, fake, n.value, None) == qsa.ERR_INVALID_ARG
     assert qsa.lib.qsa_sparse_attn_rows(ctypes.byref(d), fake, fake, fake, None, None, None, fake, fake, n.value,
