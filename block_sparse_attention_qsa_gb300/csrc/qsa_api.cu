@@ -80,6 +80,13 @@ qsa_status check_ws(const qsa_dims* d, void* ws, size_t ws_bytes, WsLayout* out)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// every non-null pointer is a multiple of `a` bytes (a power of two); the
+// kernels' scalar loads and stores of 4-byte and 2-byte elements need it
+template <typename... P>
+bool aligned_all(uintptr_t a, P... ps) {
+  return ((ps == nullptr || (reinterpret_cast<uintptr_t>(ps) & (a - 1)) == 0) && ...);
+}
+
 qsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA; }
 
 inline int32_t* err_word(void* ws) { return static_cast<int32_t*>(ws); }
@@ -146,7 +153,7 @@ qsa_status qsa_compress_keys(const qsa_dims* dims, const void* idx_keys, const i
   if (st != QSA_OK) return st;
   if (dims->batch > 65535) return QSA_ERR_UNSUPPORTED;  // one grid row (y) per request
   if (!idx_keys || !q_pos || !kc) return QSA_ERR_INVALID_ARG;
-  if (!aligned16(idx_keys) || !aligned16(kc)) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(idx_keys) || !aligned16(kc) || !aligned_all(4, q_pos, block_lo)) return QSA_ERR_INVALID_ARG;
   if ((st = check_ws(dims, ws, ws_bytes, nullptr)) != QSA_OK) return st;
   cudaError_t e = launch_compress(*dims, static_cast<const __nv_bfloat16*>(idx_keys), q_pos, block_lo,
                                   static_cast<__nv_bfloat16*>(kc), err_word(ws),
@@ -161,7 +168,7 @@ qsa_status qsa_compress_keys_paged(const qsa_dims* dims, const void* idx_keys, c
   if (st != QSA_OK) return st;
   if (dims->batch > 65535) return QSA_ERR_UNSUPPORTED;  // one grid row (y) per request
   if (!idx_keys || !q_pos || !page_table || !kc_cache) return QSA_ERR_INVALID_ARG;
-  if (!aligned16(idx_keys) || !aligned16(kc_cache)) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(idx_keys) || !aligned16(kc_cache) || !aligned_all(4, q_pos, page_table)) return QSA_ERR_INVALID_ARG;
   if ((st = check_ws(dims, ws, ws_bytes, nullptr)) != QSA_OK) return st;
   return from_cuda(launch_compress(*dims, static_cast<const __nv_bfloat16*>(idx_keys), q_pos, block_lo,
                                    static_cast<__nv_bfloat16*>(kc_cache), err_word(ws),
@@ -175,7 +182,8 @@ qsa_status qsa_score_paged(const qsa_dims* dims, const void* q_idx, const void* 
   if (st != QSA_OK) return st;
   if (dims->batch > QSA_MAX_SCORE_BATCH) return QSA_ERR_UNSUPPORTED;  // per-request tables in shared memory
   if (!q_idx || !kc_cache || !page_table || !q_pos || !scores) return QSA_ERR_INVALID_ARG;
-  if (!aligned16(q_idx) || !aligned16(kc_cache)) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(kc_cache) || !aligned_all(4, page_table, q_pos, scores))
+    return QSA_ERR_INVALID_ARG;
   if ((st = check_ws(dims, ws, ws_bytes, nullptr)) != QSA_OK) return st;
   return from_cuda(launch_score(*dims, static_cast<const __nv_bfloat16*>(q_idx),
                                 static_cast<const __nv_bfloat16*>(kc_cache), q_pos, scores, err_word(ws),
@@ -188,7 +196,7 @@ qsa_status qsa_score(const qsa_dims* dims, const void* q_idx, const void* kc, co
   if (st != QSA_OK) return st;
   if (dims->batch > QSA_MAX_SCORE_BATCH) return QSA_ERR_UNSUPPORTED;  // per-request tables in shared memory
   if (!q_idx || !kc || !q_pos || !scores) return QSA_ERR_INVALID_ARG;
-  if (!aligned16(q_idx) || !aligned16(kc)) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(kc) || !aligned_all(4, q_pos, scores)) return QSA_ERR_INVALID_ARG;
   if ((st = check_ws(dims, ws, ws_bytes, nullptr)) != QSA_OK) return st;
   return from_cuda(launch_score(*dims, static_cast<const __nv_bfloat16*>(q_idx),
                                 static_cast<const __nv_bfloat16*>(kc), q_pos, scores, err_word(ws),
@@ -201,7 +209,7 @@ qsa_status qsa_score_chunk(const qsa_dims* dims, int32_t n_chunk, const void* q_
   if (st != QSA_OK) return st;
   if (n_chunk < 1 || n_chunk > QSA_MAX_CHUNK) return QSA_ERR_INVALID_ARG;
   if (!q_idx || !kc || !q_pos || !scores) return QSA_ERR_INVALID_ARG;
-  if (!aligned16(q_idx) || !aligned16(kc)) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(kc) || !aligned_all(4, q_pos, scores)) return QSA_ERR_INVALID_ARG;
   if ((long long)dims->batch * n_chunk * dims->max_blocks >= (1LL << 40)) return QSA_ERR_UNSUPPORTED;
   if (dims->batch > 65535) return QSA_ERR_UNSUPPORTED;  // one grid row (z) per request
   if ((st = check_ws(dims, ws, ws_bytes, nullptr)) != QSA_OK) return st;
@@ -215,6 +223,7 @@ qsa_status qsa_topk(const qsa_dims* dims, const float* scores, const int32_t* q_
   qsa_status st = check_dims(dims);
   if (st != QSA_OK) return st;
   if (!scores || !q_pos || !sel_blk || !sel_pos) return QSA_ERR_INVALID_ARG;
+  if (!aligned_all(4, scores, q_pos, sel_blk, sel_pos)) return QSA_ERR_INVALID_ARG;
   if ((st = check_ws(dims, ws, ws_bytes, nullptr)) != QSA_OK) return st;
   return from_cuda(launch_topk(*dims, scores, q_pos, sel_blk, sel_pos, err_word(ws), nullptr, nullptr,
                                static_cast<cudaStream_t>(stream), false));
@@ -230,6 +239,8 @@ qsa_status qsa_sparse_attn(const qsa_dims* dims, const void* q, const void* k_ca
     return QSA_ERR_INVALID_ARG;
   if (dims->kv_dtype == QSA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return QSA_ERR_INVALID_ARG;
   if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q))
+    return QSA_ERR_INVALID_ARG;
+  if (!aligned_all(4, k_scale, v_scale, page_table, sel_pos, q_pos) || !aligned_all(2, out))
     return QSA_ERR_INVALID_ARG;
   WsLayout w;
   if ((st = check_ws(dims, ws, ws_bytes, &w)) != QSA_OK) return st;
@@ -247,6 +258,7 @@ qsa_status qsa_resolve(const qsa_dims* dims, const int32_t* sel_pos, const int32
   qsa_status st = check_dims(dims);
   if (st != QSA_OK) return st;
   if (!sel_pos || !q_pos || !page_table || !sel_row) return QSA_ERR_INVALID_ARG;
+  if (!aligned_all(4, sel_pos, q_pos, page_table, sel_row)) return QSA_ERR_INVALID_ARG;
   if ((st = check_ws(dims, ws, ws_bytes, nullptr)) != QSA_OK) return st;
   return from_cuda(launch_resolve(*dims, sel_pos, q_pos, page_table, sel_row, err_word(ws),
                                   static_cast<cudaStream_t>(stream)));
@@ -261,6 +273,7 @@ qsa_status qsa_sparse_attn_rows(const qsa_dims* dims, const void* q, const void*
   if (dims->kv_dtype == QSA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return QSA_ERR_INVALID_ARG;
   if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q))
     return QSA_ERR_INVALID_ARG;
+  if (!aligned_all(4, k_scale, v_scale, sel_row) || !aligned_all(2, out)) return QSA_ERR_INVALID_ARG;
   WsLayout w;
   if ((st = check_ws(dims, ws, ws_bytes, &w)) != QSA_OK) return st;
   const AttnPlan pl{w.units, w.tiles, w.grid};
@@ -286,6 +299,8 @@ qsa_status decode_impl(const qsa_dims* dims, const void* q_idx, const void* kc, 
   if (dims->kv_dtype == QSA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return QSA_ERR_INVALID_ARG;
   if (!aligned16(q_idx) || !aligned16(kc) || !aligned16(k_cache) || !aligned16(v_cache) ||
       !aligned16(q))
+    return QSA_ERR_INVALID_ARG;
+  if (!aligned_all(4, k_scale, v_scale, page_table, q_pos, scores, sel_blk, sel_pos) || !aligned_all(2, out))
     return QSA_ERR_INVALID_ARG;
   WsLayout w;
   if ((st = check_ws(dims, ws, ws_bytes, &w)) != QSA_OK) return st;
@@ -338,6 +353,8 @@ qsa_status qsa_draft_attn(const qsa_dims* dims, const void* q, const void* k_cac
   if (n_sel < 1 || n_sel > kMaxNq) return QSA_ERR_INVALID_ARG;
   if (dims->kv_dtype == QSA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return QSA_ERR_INVALID_ARG;
   if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q))
+    return QSA_ERR_INVALID_ARG;
+  if (!aligned_all(4, k_scale, v_scale, page_table, sel_pos, sel_q_pos, src, q_pos) || !aligned_all(2, out))
     return QSA_ERR_INVALID_ARG;
   WsLayout w;
   if ((st = check_ws(dims, ws, ws_bytes, &w)) != QSA_OK) return st;

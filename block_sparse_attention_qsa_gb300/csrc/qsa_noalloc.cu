@@ -12,6 +12,8 @@
 // process exits.
 #include <mutex>
 
+#include <initializer_list>
+
 #include "qsa_internal.cuh"
 
 namespace {
@@ -58,6 +60,12 @@ extern "C" qsa_status qsa_sparse_attn_noalloc(const qsa_dims* dims, const void* 
   if ((reinterpret_cast<uintptr_t>(k_cache) & 15u) || (reinterpret_cast<uintptr_t>(v_cache) & 15u) ||
       (reinterpret_cast<uintptr_t>(q) & 15u))
     return QSA_ERR_INVALID_ARG;
+  // 4-byte and 2-byte elements: their scalar loads and stores need that alignment
+  for (const void* p4 : {static_cast<const void*>(k_scale), static_cast<const void*>(v_scale),
+                         static_cast<const void*>(page_table), static_cast<const void*>(sel_pos),
+                         static_cast<const void*>(q_pos)})
+    if (reinterpret_cast<uintptr_t>(p4) & 3u) return QSA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(out) & 1u) return QSA_ERR_INVALID_ARG;
 
   // The usual plan, with fewer CTAs (so fewer partials) if it would not fit.
   qsa::AttnPlan plan = qsa::attn_plan(*dims, qsa::device_sm_count());

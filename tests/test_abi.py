@@ -99,6 +99,11 @@ def test_workspace_size_and_rejections_need_no_gpu(qsa):
                                    n.value, None) == qsa.ERR_INVALID_ARG
     assert qsa.lib.qsa_sparse_attn_rows(ctypes.byref(d), q4, fake, fake, None, None, fake, fake, fake, n.value,
                                         None) == qsa.ERR_INVALID_ARG
+    # 4-byte and 2-byte elements need their own alignment
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    assert qsa.lib.qsa_score(ctypes.byref(d), fake, fake, odd, fake, fake, n.value, None) == qsa.ERR_INVALID_ARG
+    assert qsa.lib.qsa_sparse_attn_rows(ctypes.byref(d), fake, fake, fake, None, None, fake,
+                                        ctypes.c_void_p((1 << 20) + 1), fake, n.value, None) == qsa.ERR_INVALID_ARG
     # resolve / attention over rows: null pointers
     assert qsa.lib.qsa_resolve(ctypes.byref(d), fake, fake, None, fake, fake, n.value, None) == qsa.ERR_INVALID_ARG
     assert qsa.lib.qsa_sparse_attn_rows(ctypes.byref(d), fake, fake, fake, None, None, None, fake, fake, n.value,
