@@ -803,6 +803,41 @@ def test_uniform_v_gives_v(qsa):
     assert torch.max(torch.abs(out.float() - row.float())).item() <= 1e-2
 
 
+def test_fp8_every_code_through_attention(qsa):
+    # Attention over one selected position returns that position's V row. With
+    # V rows holding every finite E4M3 code (the two NaN codes set to 0), the
+    # kernel's packed FP8 -> FP16 widening must reproduce the OCP decode of each
+    # code exactly (every E4M3 value is exact in FP16 and in BF16).
+    spec = synth.Spec("fp8-codes", 1, 2, [40], 1, "fp8", True, 61)
+    g = _dev(synth.make_inputs(spec))
+    codes = np.arange(256, dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0
+    pt = g["page_table"][0].long()
+    page0 = int(pt[0].item())
+    v = g["v_cache"]
+    for h in range(spec.n_kv_heads):
+        # token 0: codes 0..127; token 1: codes 128..255 (both KV heads, rolled so heads differ)
+        v[page0, h, 0] = torch.from_numpy(np.roll(codes[:128], 17 * h).copy()).cuda()
+        v[page0, h, 1] = torch.from_numpy(np.roll(codes[128:], 17 * h).copy()).cuda()
+    g["k_scale"][:] = 1.0
+    g["v_scale"][:] = 1.0
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    sel = torch.full((1, 2, 2051), -1, dtype=torch.int32, device="cuda")
+    sel[0, 0, 0] = 0  # query 0 attends to token 0 only
+    sel[0, 1, 0] = 1  # query 1 to token 1 only
+    out = torch.empty((1, 2, 16, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.sparse_attn(d, g["q"], g["k_cache"], v, g["k_scale"], g["v_scale"], g["page_table"], sel, g["q_pos"], out,
+                    ws)
+    _check_ok(qsa, ws)
+    got = out.float().cpu().numpy()
+    vh = v.cpu().numpy()
+    for j, tok in ((0, 0), (1, 1)):
+        for hq in range(16):
+            want = O.e4m3_to_f64(vh[page0, hq // 8, tok])
+            assert np.array_equal(got[0, j, hq], want), (j, hq)
+
+
 def test_device_errors_are_reported_not_fatal(qsa):
     spec = small_spec([3000, 2000], n_q=2, seed=34)
     g = _dev(synth.make_inputs(spec))
