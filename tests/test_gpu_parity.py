@@ -838,6 +838,50 @@ def test_fp8_every_code_through_attention(qsa):
             assert np.array_equal(got[0, j, hq], want), (j, hq)
 
 
+def test_bf16_single_position_returns_its_v_row_exactly(qsa):
+    # softmax over one position has weight 1: the output is the V row itself
+    spec = synth.Spec("bf16-one", 1, 2, [40], 1, "bf16", True, 62)
+    g = _dev(synth.make_inputs(spec))
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    sel = torch.full((1, 2, 2051), -1, dtype=torch.int32, device="cuda")
+    sel[0, 0, 0] = 5
+    sel[0, 1, 0] = 41  # the query's own token
+    out = torch.empty((1, 2, 16, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.sparse_attn(d, g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"], g["page_table"], sel,
+                    g["q_pos"], out, ws)
+    _check_ok(qsa, ws)
+    pt = g["page_table"][0]
+    for j, tok in ((0, 5), (1, 41)):
+        page = int(pt[tok // spec.page_size].item())
+        for hq in range(16):
+            row = g["v_cache"][page, hq // 8, tok % spec.page_size]
+            assert torch.equal(out[0, j, hq].view(torch.int16), row.view(torch.int16)), (j, hq)
+
+
+@pytest.mark.parametrize("h", [1, 2])
+def test_one_hot_query_reads_one_key_dimension(qsa, h):
+    # closed form: a query equal to 1 at (head hh, dim dd) and 0 elsewhere
+    # scores each block with exactly its compressed key's (hh, dd) component
+    spec = small_spec([3001, 1498], n_q=4, n_idx_heads=h, seed=63)
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    mb = spec.max_blocks()
+    kc = synth.normal_bf16((spec.batch, mb, h, 128), 64, "cuda")
+    picks = [(j % h, (37 * j + 5) % 128) for j in range(4)]
+    q_idx = torch.zeros((spec.batch, 4, h, 128), dtype=torch.bfloat16, device="cuda")
+    for j, (hh, dd) in enumerate(picks):
+        q_idx[:, j, hh, dd] = 1.0
+    q_pos = torch.tensor(spec.q_pos(), dtype=torch.int32, device="cuda")
+    scores = torch.full((spec.batch, 4, mb), float("nan"), device="cuda")
+    qsa.score(d, q_idx, kc, q_pos, scores, ws)
+    _check_ok(qsa, ws)
+    for r in range(spec.batch):
+        for j, (hh, dd) in enumerate(picks):
+            nb = O.n_full(spec.q_pos()[r][j])
+            assert torch.equal(scores[r, j, :nb], kc[r, :nb, hh, dd].float()), (r, j)
+
+
 def test_device_errors_are_reported_not_fatal(qsa):
     spec = small_spec([3000, 2000], n_q=2, seed=34)
     g = _dev(synth.make_inputs(spec))
