@@ -882,6 +882,45 @@ def test_one_hot_query_reads_one_key_dimension(qsa, h):
             assert torch.equal(scores[r, j, :nb], kc[r, :nb, hh, dd].float()), (r, j)
 
 
+def test_compressed_key_of_identical_tokens_is_the_token_key(qsa):
+    # closed form: the FP32 mean of four equal BF16 values is that value exactly
+    spec = small_spec([2001, 777], n_q=2, n_idx_heads=2, seed=65)
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    mb = spec.max_blocks()
+    base = synth.normal_bf16((spec.batch, mb, 2, 128), 66, "cuda")
+    idx_keys = base.repeat_interleave(4, dim=1).contiguous()  # [B][4 mb][2][128]: 4 equal tokens per block
+    q_pos = torch.tensor(spec.q_pos(), dtype=torch.int32, device="cuda")
+    kc = torch.zeros_like(base)
+    qsa.compress_keys(d, idx_keys, q_pos, kc, ws)
+    _check_ok(qsa, ws)
+    for r in range(spec.batch):
+        nb = O.n_full(max(spec.q_pos()[r]))
+        assert torch.equal(kc[r, :nb].view(torch.int16), base[r, :nb].view(torch.int16)), r
+
+
+def test_chunk_one_hot_queries_read_one_key_dimension(qsa):
+    spec = small_spec([3001], n_q=1, n_idx_heads=2, seed=67)
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    mb = spec.max_blocks()
+    n_chunk = 70  # two query tiles, the second ragged
+    kc = synth.normal_bf16((1, mb, 2, 128), 68, "cuda")
+    q_idx = torch.zeros((1, n_chunk, 2, 128), dtype=torch.bfloat16, device="cuda")
+    picks = [(i % 2, (29 * i + 3) % 128) for i in range(n_chunk)]
+    for i, (hh, dd) in enumerate(picks):
+        q_idx[0, i, hh, dd] = 1.0
+    pos = [2999 - 7 * i for i in range(n_chunk)]
+    q_pos = torch.tensor([pos], dtype=torch.int32, device="cuda")
+    scores = torch.full((1, n_chunk, mb), float("nan"), device="cuda")
+    qsa.score_chunk(d, q_idx, kc, q_pos, scores, ws)
+    _check_ok(qsa, ws)
+    for i, (hh, dd) in enumerate(picks):
+        nb = O.n_full(pos[i])
+        assert torch.equal(scores[0, i, :nb], kc[0, :nb, hh, dd].float()), i
+        assert torch.all(torch.isnan(scores[0, i, nb:]))
+
+
 def test_device_errors_are_reported_not_fatal(qsa):
     spec = small_spec([3000, 2000], n_q=2, seed=34)
     g = _dev(synth.make_inputs(spec))
