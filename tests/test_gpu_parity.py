@@ -921,6 +921,44 @@ def test_chunk_one_hot_queries_read_one_key_dimension(qsa):
         assert torch.all(torch.isnan(scores[0, i, nb:]))
 
 
+@pytest.mark.parametrize("config,kv", [(1, "bf16"), (3, "fp8")])
+def test_zero_keys_give_the_mean_of_v_over_the_selection(qsa, config, kv):
+    # closed form: with every key zero all scores tie, so each output is the
+    # plain mean of V over the query's selected positions; at batch 1 a unit is
+    # cut into about 17 pieces, so this checks the merge of pieces as well
+    spec = synth.spec_for(config, batch=1) if config == 3 else synth.spec_for(config)
+    g = synth.make_inputs(spec, device="cuda")
+    g["k_cache"].zero_()
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    rng = np.random.default_rng(69)
+    sel = torch.full((1, 4, 2051), -1, dtype=torch.int32)
+    for j in range(4):
+        p = spec.q_pos()[0][j]
+        pick = np.sort(rng.choice(p + 1, size=2051, replace=False))
+        sel[0, j] = torch.from_numpy(pick.astype(np.int32))
+    sel = sel.cuda()
+    out = torch.empty((1, 4, 16, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.sparse_attn(d, g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"], g["page_table"], sel,
+                    g["q_pos"], out, ws)
+    _check_ok(qsa, ws)
+    P = spec.page_size
+    pt = g["page_table"][0].long()
+    for j in range(4):
+        t = sel[0, j].long()
+        pages, slots = pt[t // P], t % P
+        for kvh in range(2):
+            rows = g["v_cache"][pages, kvh, slots]
+            if kv == "fp8":
+                vals = torch.from_numpy(O.e4m3_to_f64(rows.cpu().numpy())) * float(g["v_scale"][kvh].item())
+            else:
+                vals = rows.double().cpu()
+            mean = vals.mean(dim=0)
+            for hq in range(8 * kvh, 8 * kvh + 8):
+                err = (out[0, j, hq].double().cpu() - mean).abs().max().item()
+                assert err <= ATOL[kv], (j, hq, err)
+
+
 def test_device_errors_are_reported_not_fatal(qsa):
     spec = small_spec([3000, 2000], n_q=2, seed=34)
     g = _dev(synth.make_inputs(spec))
