@@ -51,10 +51,13 @@ template <bool FP8>
 constexpr int kCtasPerSm = 3;
 template <bool FP8>
 constexpr int kRowsPerLane = FP8 ? 4 : 2;
-// Small batches: each CTA takes at least this many tiles, so a unit is cut
-// into at most 17 pieces and the merge of the last piece to arrive stays short
-// (measured at batch 1: 1 tile 35.1 us per step, 2 tiles 32.2, 4 tiles 33.5).
-constexpr int kMinTilesPerCta = 2;
+// Small batches: each CTA takes at least this many tiles (192 BF16 or 256 FP8
+// positions), so a unit is cut into few pieces and the merge of the last one
+// to arrive stays short. Measured at batch 1, BF16: 1 tile 35.1 us per step,
+// 2 tiles 30.7, 3 tiles 28.9, 4 tiles 33.5 (the first and last with an older
+// build); FP8 (tiles twice as long): 2 tiles 31.0, 3 tiles 32.1.
+template <bool FP8>
+constexpr int kMinTilesPerCta = FP8 ? 2 : 3;
 constexpr int kMergeBatch = 4;  // pieces whose accumulators are read at once
 constexpr int kThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -688,7 +691,8 @@ AttnPlan attn_plan(const qsa_dims& d, int num_sms) {
   const long long total = (long long)pl.units * pl.tiles;
   const long long resident =
       (long long)(d.kv_dtype == QSA_KV_FP8_E4M3 ? kCtasPerSm<true> : kCtasPerSm<false>) * num_sms;
-  const long long most = (total + kMinTilesPerCta - 1) / kMinTilesPerCta;
+  const int min_tiles = d.kv_dtype == QSA_KV_FP8_E4M3 ? kMinTilesPerCta<true> : kMinTilesPerCta<false>;
+  const long long most = (total + min_tiles - 1) / min_tiles;
   pl.grid = (int)(most < resident ? most : resident);
   return pl;
 }
