@@ -13,6 +13,11 @@ L2 is flushed before every timed step (a write of twice its size, then a read
 of another buffer that size, so the lines the write leaves dirty are written
 back before the timed region); the flush is outside the timed events.
 
+The same run also times a sweep (batches 1-32 of the 50K-token verify step
+with BF16 KV, batches 1 and 32 with FP8 KV, and the long-context workload at
+131,072 tokens) and the CPU oracle, on one core and on all of the host's
+cores.
+
     python bench.py [--steps K] [--warmup W] [--config {0,1,2,3,4}] [--impl reference]
 """
 
@@ -41,6 +46,11 @@ from block_sparse_attention_qsa_gb300 import synth  # noqa: E402
 
 METRIC = "QSA step latency (µs) and HBM GB/s, batch 1–32, 50K ctx, 4 verify queries"
 UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0  # the HBM3e figure the target is also quoted against (nominal, not measured)
+
+# the sweep of the metric: (config, batch, context) beside the headline
+SWEEP = [(2, 1, None), (2, 2, None), (2, 4, None), (2, 8, None), (2, 16, None), (2, 32, None),
+         (3, 1, None), (3, 32, None), (4, 1, 131072), (4, 8, 131072)]
 
 
 def parse_args():
@@ -66,6 +76,10 @@ def parse_args():
     ap.add_argument("--draft", action="store_true",
                     help="time an MTP draft step instead: one draft query per request attending over the "
                          "selection of the request's first verify query plus the 3 positions after it")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the batch / cache-type sweep")
+    ap.add_argument("--sweep-steps", type=int, default=100, help="timed steps per sweep entry")
+    ap.add_argument("--cpu-requests", type=int, default=8,
+                    help="requests of the batch saved for the all-core oracle timing (cycled)")
     return ap.parse_args()
 
 
@@ -416,13 +430,13 @@ def run_chunk(qsa, args, world, rank):
                           "l2": "no flush (warm)" if flush is None else "flushed before every call"}))
 
 
-def run_ours(args, world, rank):
-    qsa = build_lib()
-    if args.chunk:
-        return run_chunk(qsa, args, world, rank)
-    spec = synth.spec_for(args.config, batch=args.batch, ctx=args.ctx, replica=rank)
+def prepare_step(qsa, spec, paged_kc=False):
+    """Device state of one workload and one checked step, whose selection
+    gives the algorithmic byte count. Returns (state, sel_pos on the host,
+    compressed-key bytes, K/V bytes of the union per request, K/V bytes
+    summed over queries)."""
     st = make_gpu_state(qsa, spec)
-    if args.paged_kc:
+    if paged_kc:
         g = st["g"]
         kcp = torch.zeros((spec.num_pages(), spec.page_size // 4, spec.n_idx_heads, spec.head_dim),
                           dtype=torch.bfloat16, device="cuda")
@@ -431,46 +445,125 @@ def run_ours(args, world, rank):
         qsa.compress_keys_paged(st["d"], idx_keys, g["q_pos"], g["page_table"], kcp, st["ws"])
         del idx_keys
         st["kc"], st["paged_kc"] = kcp, True
+    g = st["g"]
+    (qsa.decode_paged if paged_kc else qsa.decode)(
+        st["d"], g["q_idx"], st["kc"], g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"],
+        g["page_table"], g["q_pos"], st["out"], st["ws"], scores=st["scores"], sel_blk=st["sel_blk"],
+        sel_pos=st["sel_pos"])
+    status, info = qsa.check_errors(st["ws"])
+    if status != qsa.OK:
+        raise RuntimeError(f"device error during the step: {info}")
+    sel_host = st["sel_pos"].cpu().numpy()
+    b_kv_union, b_kv_sum = kv_bytes(spec, sel_host)
+    return st, sel_host, kc_bytes(spec), b_kv_union, b_kv_sum
+
+
+def step_launcher(qsa, st, graph):
+    """The timed step: qsa_decode captured once as a CUDA graph (its three
+    kernels and their programmatic dependencies) and replayed, as a serving
+    loop would run it, or direct calls."""
+    if not graph:
+        return lambda: decode_call(qsa, st)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            decode_call(qsa, st)
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        decode_call(qsa, st)
+    st["graph"] = g
+    return g.replay
+
+
+def warm(fn, n, flush):
+    for _ in range(n):
+        if flush is not None:
+            flush()
+        fn()
+    torch.cuda.synchronize()
+
+
+def sweep(qsa, args, flush, stream, peak, headline):
+    """Step latency and algorithmic GB/s over the metric's batches and cache
+    types, each entry its own workload (inputs drawn for that batch)."""
+    out = []
+    for config, batch, ctx in SWEEP:
+        if headline is not None and (config, batch, ctx) == headline[0]:
+            out.append(dict(headline[1], reused="the headline measurement"))
+            continue
+        spec = synth.spec_for(config, batch=batch, ctx=ctx)
+        st, _, b_kc, b_kv, _ = prepare_step(qsa, spec)
+        fn = step_launcher(qsa, st, not args.no_graph)
+        warm(fn, max(3, args.warmup), flush)
+        ms = timed(fn, args.sweep_steps, flush, stream)
+        out.append(sweep_entry(spec, config, ms, b_kc + b_kv, peak))
+        del st, fn
+        torch.cuda.empty_cache()
+    return out
+
+
+def sweep_entry(spec, config, ms_list, bytes_step, peak):
+    ms = sum(ms_list) / len(ms_list)
+    gbs = bytes_step / (ms * 1e-3) / 1e9
+    return {"workload": spec.name, "config": config, "batch": spec.batch, "kv": spec.kv_dtype,
+            "context": "50000+800*t, t~U{0..14}" if config in (2, 3) else spec.first_pos[0],
+            "us_mean": round(ms * 1e3, 2), "us_p50": round(float(np.percentile(ms_list, 50)) * 1e3, 2),
+            "steps": len(ms_list), "alg_bytes": int(bytes_step), "gbs": round(gbs, 1),
+            "frac_of_measured_peak": round(gbs / peak, 4), "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)}
+
+
+def oracle_all_cores(spec, src, idx_keys_fn, n_saved, seconds, t_req_single):
+    """The oracle on every host core: whole requests of the workload (the
+    first n_saved of the batch, cycled) run one per process on a spawn-context
+    pool, inputs memory-mapped from files written before the timing. Returns
+    (bytes, seconds, requests, workers)."""
+    import shutil
+    import tempfile
+
+    from oracle import parallel as OP
+    from oracle import qsa_oracle as O
+
+    workers = OP.host_cores()
+    tmp = tempfile.mkdtemp(prefix="qsa_oracle_")
+    try:
+        n_saved = max(1, min(n_saved, spec.batch))
+        for r in range(n_saved):
+            npi = host_request(spec, src, r)
+            npi["kc"] = O.compress_keys(idx_keys_fn(r), spec.max_blocks())[None]
+            OP.save_request(tmp, r, npi)
+        pool = OP.OraclePool(workers)
+        try:
+            pool.timed(tmp, range(min(workers, n_saved)), spec.kv_dtype, kv_row_bytes(spec))  # page the files in
+            n = max(workers, int(seconds * workers / max(t_req_single, 1e-3)))
+            b, s, done = pool.timed(tmp, [i % n_saved for i in range(n)], spec.kv_dtype, kv_row_bytes(spec))
+        finally:
+            pool.close()
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
+    return b, s, done, workers
+
+
+def run_ours(args, world, rank):
+    qsa = build_lib()
+    if args.chunk:
+        return run_chunk(qsa, args, world, rank)
+    spec = synth.spec_for(args.config, batch=args.batch, ctx=args.ctx, replica=rank)
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     flush = None if args.no_flush else L2Flush(l2)
 
     # one checked step: its selection gives the byte count
+    st, sel_host, b_kc, b_kv_union, b_kv_sum = prepare_step(qsa, spec, args.paged_kc)
     d = st["d"]
-    (qsa.decode_paged if args.paged_kc else qsa.decode)(
-        d, st["g"]["q_idx"], st["kc"], st["g"]["q"], st["g"]["k_cache"], st["g"]["v_cache"], st["g"]["k_scale"],
-        st["g"]["v_scale"], st["g"]["page_table"], st["g"]["q_pos"], st["out"], st["ws"], scores=st["scores"],
-        sel_blk=st["sel_blk"], sel_pos=st["sel_pos"])
-    status, info = qsa.check_errors(st["ws"])
-    if status != qsa.OK:
-        raise RuntimeError(f"device error during the step: {info}")
-    sel_host = st["sel_pos"].cpu().numpy()
-    b_kc = kc_bytes(spec)
-    b_kv_union, b_kv_sum = kv_bytes(spec, sel_host)
     bytes_step = b_kc + b_kv_union
     if args.draft:
         return run_draft(qsa, args, spec, st, sel_host, flush, stream, world, rank)
 
-    # warm-up, then exactly K timed steps. The step is captured once as a CUDA
-    # graph (its three kernels and their programmatic dependencies), as a
-    # serving loop would run it, and replayed; --no-graph times direct calls.
-    step_fn = lambda: decode_call(qsa, st)
-    if not args.no_graph:
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            for _ in range(3):
-                decode_call(qsa, st)
-        torch.cuda.current_stream().wait_stream(side)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            decode_call(qsa, st)
-        step_fn = graph.replay
-    for _ in range(args.warmup):
-        if flush is not None:
-            flush()
-        step_fn()
-    torch.cuda.synchronize()
+    # warm-up, then exactly K timed steps
+    step_fn = step_launcher(qsa, st, not args.no_graph)
+    warm(step_fn, args.warmup, flush)
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -528,7 +621,8 @@ def run_ours(args, world, rank):
     roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
                 "traffic": traffic, "alg_bytes_per_launch": int(k_bytes[dom]),
-                "step_frac": round(value / world / peak, 4)}
+                "step_frac": round(value / world / peak, 4),
+                "step_frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4)}
 
     # end to end through the public API with host buffers: the step's inputs
     # (index queries, queries, positions, page table) live in one pinned host
@@ -580,16 +674,30 @@ def run_ours(args, world, rank):
            "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
            "launch": "direct calls" if args.no_graph else "copies and step captured once as a CUDA graph, replayed"}
 
-    cpu = None
+    cpu, cpu1 = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         idx_keys = synth.normal_bf16((spec.batch, 4 * spec.max_blocks(), spec.n_idx_heads, spec.head_dim),
                                      spec.seed + synth.T_IDXKEYS, device="cuda")
-        b, s, n = oracle_steps(spec, g, lambda r: _bits(idx_keys[r]), seconds=args.cpu_seconds)
+        kfn = lambda r: _bits(idx_keys[r])  # noqa: E731
+        b1, s1, n1 = oracle_steps(spec, g, kfn, seconds=args.cpu_seconds)
+        cpu1 = {"value": round(b1 / s1 / 1e9, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"{n1} requests of the {spec.batch}-request batch (cycling), all {spec.n_q} queries each, "
+                          f"one at a time, numpy FP64, one thread", "seconds": round(s1, 2)}
+        bn, sn, nn, workers = oracle_all_cores(spec, g, kfn, args.cpu_requests, args.cpu_seconds, s1 / n1)
         del idx_keys
-        cpu = {"value": round(b / s / 1e9, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{n} requests of the {spec.batch}-request batch (cycling), all {spec.n_q} queries each, "
-                         f"one at a time, numpy FP64",
-               "seconds": round(s, 2)}
+        cpu = {"value": round(bn / sn / 1e9, 6), "unit": UNIT, "cores": workers, "kind": "oracle",
+               "sample": f"{nn} requests (the first {min(args.cpu_requests, spec.batch)} of the "
+                         f"{spec.batch}-request batch, cycled), all {spec.n_q} queries each, one request per "
+                         f"process on {workers} processes (spawn), numpy FP64",
+               "seconds": round(sn, 2), "host_cpu_count": os.cpu_count()}
+
+    sweep_out = None
+    if not args.no_sweep and world == 1 and args.config in (2, 3) and not args.paged_kc:
+        headline_entry = sweep_entry(spec, args.config, step_ms, bytes_step, peak)
+        key = (args.config, spec.batch, None)
+        del st, step_fn, rows, host_buf, dev_buf, dev_in, out_host, e2e_fn
+        torch.cuda.empty_cache()
+        sweep_out = sweep(qsa, args, flush, stream, peak, (key, headline_entry))
 
     if rank == 0:
         res = {
@@ -607,33 +715,67 @@ def run_ours(args, world, rank):
                        "parallelism": f"replicas x{world}"},
             "bytes_per_step": {"kc": int(b_kc), "kv_union": int(b_kv_union), "kv_sum": int(b_kv_sum)},
             "kernels": kernels, "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
+            "cpu_baseline_single_core": cpu1, "sweep": sweep_out,
             "gpu_launches": 3 * args.steps, "clocks": clocks,
         }
         print(json.dumps(res))
 
 
 def run_reference(args, world, rank):
-    """The oracle as it stands, timed on the host cores, one request per step."""
+    """The oracle as it stands, timed on the host's cores: each step runs as
+    many whole requests of the workload as there are cores, one per process."""
     if rank != 0:
         return
+    import shutil
+    import tempfile
+
+    from oracle import parallel as OP
+    from oracle import qsa_oracle as O
+
     spec = synth.spec_for(args.config, batch=args.batch, ctx=args.ctx)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     g = synth.make_inputs(spec, device=dev, with_index_keys=False)
     idx_keys = synth.normal_bf16((spec.batch, 4 * spec.max_blocks(), spec.n_idx_heads, spec.head_dim),
                                  spec.seed + synth.T_IDXKEYS, device=dev)
-    kfn = lambda r: _bits(idx_keys[r])  # noqa: E731
-    oracle_steps(spec, g, kfn, n_steps=args.warmup)
-    b, s, n = oracle_steps(spec, g, kfn, n_steps=args.steps)
+    workers = OP.host_cores()
+    per_step = workers  # one whole request per process each step, cycling over the batch
+    n_saved = max(1, min(spec.batch, args.cpu_requests))
+    tmp = tempfile.mkdtemp(prefix="qsa_oracle_")
+    try:
+        for r in range(n_saved):
+            npi = host_request(spec, g, r)
+            npi["kc"] = O.compress_keys(_bits(idx_keys[r]), spec.max_blocks())[None]
+            OP.save_request(tmp, r, npi)
+        del idx_keys, g
+        pool = OP.OraclePool(workers)
+        try:
+            nxt = 0
+            for _ in range(args.warmup):
+                pool.timed(tmp, [(nxt + i) % n_saved for i in range(per_step)], spec.kv_dtype, kv_row_bytes(spec))
+                nxt += per_step
+            b = s = n = 0
+            for _ in range(args.steps):
+                bb, ss, nn = pool.timed(tmp, [(nxt + i) % n_saved for i in range(per_step)], spec.kv_dtype,
+                                        kv_row_bytes(spec))
+                nxt += per_step
+                b, s, n = b + bb, s + ss, n + nn
+        finally:
+            pool.close()
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
     value = b / s / 1e9
     res = {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s / n * 1e3, 3),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
         "config": {"workload": spec.name, "batch": spec.batch, "n_q": spec.n_q, "kv": spec.kv_dtype,
-                   "step": "one request (all its queries) of the batch, cycling"},
-        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{n} requests of {spec.name}, one per step, numpy FP64 single-threaded"},
+                   "n_idx_heads": spec.n_idx_heads, "page_size": spec.page_size,
+                   "step": f"{per_step} whole requests of the batch (cycling over its first {n_saved}), "
+                           f"one per process"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": workers, "kind": "oracle",
+                         "sample": f"{n} requests of {spec.name}, {per_step} per step on {workers} processes "
+                                   f"(spawn), numpy FP64"},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(res))

@@ -34,7 +34,10 @@
 // Each lane looks two tiles ahead in the selection, so the K/V loads of the
 // next tile are in flight across unit boundaries. FP8 codes stay packed in
 // registers and are widened to FP16 (exact for E4M3) right before their mma;
-// K's scale folds into the softmax scale and V's into the output. The warps'
+// the BF16 query of that FP16 contraction is scaled per head by a power of
+// two into FP16's range (exact: BF16's 8 significant bits fit FP16's 11), the
+// factor folded back into the head's softmax scale like K's scale; V's scale
+// folds into the output. The warps'
 // softmax states merge through shared memory; a unit split between CTAs
 // publishes (max, sum, acc) pieces to the workspace and the last piece to
 // arrive, counted by an atomic ticket, merges them and resets the ticket, so
@@ -134,10 +137,22 @@ __device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_
       : "r"(w));
 }
 
-// BF16 pair -> FP16 pair (Q of the FP8 path)
-__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) {
-  return pack2<true>(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+// BF16 pair times f (a power of two) -> FP16 pair (Q of the FP8 path)
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w, float f) {
+  return pack2<true>(__uint_as_float(w << 16) * f, __uint_as_float(w & 0xffff0000u) * f);
 }
+
+// Exponent shift s of a query head whose largest magnitude is amax: amax *
+// 2^-s lies in [2^14, 2^15), so the head's BF16 values times 2^-s are FP16
+// values exactly (BF16 keeps 8 significant bits, FP16 11, and the range down
+// to amax * 2^-29 stays normal); the score is multiplied back by 2^s in the
+// softmax scale. Clamped so that 2^-s and 2^s are normal FP32 numbers.
+__device__ __forceinline__ int q_shift(float amax) {
+  if (!(amax > 0.f)) return 0;
+  const int e = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127;
+  return min(126, max(-126, e - 14));
+}
+__device__ __forceinline__ float pow2(int s) { return __uint_as_float((uint32_t)(127 + s) << 23); }
 
 // Register layout of one lane's share of a 128-dim row, for lane = 4g + c.
 //   BF16 rows (256 B): 4 loads of 16 B at chunks c, c+4, c+8, c+12 -> 16
@@ -305,17 +320,34 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
     __syncthreads();
 
     uint32_t qb[16];  // B fragments of the KV group's 8 query heads (head gq)
+    float qs[2] = {1.f, 1.f};  // FP8: 2^s of heads 2c4 and 2c4 + 1 (their FP16 query scaling undone)
     {
       const __nv_bfloat16* qh = sQ[buf] + gq * kDim;
       if constexpr (FP8) {
+        // the query stays BF16 in meaning: each head is scaled by a power of
+        // two into FP16's range (exact) before the FP16 contraction
+        uint32_t wd[16];
+        uint32_t amax = 0;  // largest |q| bits of this lane's 32 dims of head gq
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           const uint4 lo = *reinterpret_cast<const uint4*>(qh + 16 * (c4 + 4 * i));
           const uint4 hi = *reinterpret_cast<const uint4*>(qh + 16 * (c4 + 4 * i) + 8);
-          const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+          const uint32_t w8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) qb[8 * i + e] = bf2_to_h2(wd[e]);
+          for (int e = 0; e < 8; ++e) {
+            wd[8 * i + e] = w8[e];
+            // magnitudes of BF16 values order like their bit patterns
+            amax = max(amax, max((w8[e] << 16) & 0x7fff0000u, w8[e] & 0x7fff0000u));
+          }
         }
+        amax = max(amax, __shfl_xor_sync(kFull, amax, 1));
+        amax = max(amax, __shfl_xor_sync(kFull, amax, 2));
+        const int sh = q_shift(__uint_as_float(amax));  // head gq
+        const float down = pow2(-sh);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) qb[e] = bf2_to_h2(wd[e], down);
+        qs[0] = pow2(__shfl_sync(kFull, sh, 4 * (2 * c4)));
+        qs[1] = pow2(__shfl_sync(kFull, sh, 4 * (2 * c4 + 1)));
       } else {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -329,7 +361,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
     }
     const float kscale = FP8 ? a.k_scale[g] : 1.f;
     const float vscale = FP8 ? a.v_scale[g] : 1.f;
-    const float scale_log2 = a.sm_scale * kscale * kLog2e;
+    // per head of this lane's two score columns (FP8: times the query's 2^s)
+    const float scale_log2A = a.sm_scale * kscale * kLog2e * qs[0];
+    const float scale_log2B = a.sm_scale * kscale * kLog2e * qs[1];
 
     float m_run[2] = {kNegInf, kNegInf}, l_run[2] = {0.f, 0.f};  // heads 2c4, 2c4 + 1
     float acc[8][4];
@@ -379,10 +413,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
       float mA = kNegInf, mB = kNegInf;
 #pragma unroll
       for (int j = 0; j < R / 2; ++j) {
-        x[j][0] = ok[2 * j] ? s[j][0] * scale_log2 : kNegInf;
-        x[j][1] = ok[2 * j] ? s[j][1] * scale_log2 : kNegInf;
-        x[j][2] = ok[2 * j + 1] ? s[j][2] * scale_log2 : kNegInf;
-        x[j][3] = ok[2 * j + 1] ? s[j][3] * scale_log2 : kNegInf;
+        x[j][0] = ok[2 * j] ? s[j][0] * scale_log2A : kNegInf;
+        x[j][1] = ok[2 * j] ? s[j][1] * scale_log2B : kNegInf;
+        x[j][2] = ok[2 * j + 1] ? s[j][2] * scale_log2A : kNegInf;
+        x[j][3] = ok[2 * j + 1] ? s[j][3] * scale_log2B : kNegInf;
         mA = fmaxf(mA, fmaxf(x[j][0], x[j][2]));
         mB = fmaxf(mB, fmaxf(x[j][1], x[j][3]));
       }

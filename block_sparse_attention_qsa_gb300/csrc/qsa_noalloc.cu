@@ -10,8 +10,6 @@
 // library's own device image instead: a file-scope __device__ array of
 // kScratchBytes that every GPU which loads the library holds until the
 // process exits.
-#include <mutex>
-
 #include <initializer_list>
 
 #include "qsa_internal.cuh"
@@ -24,24 +22,16 @@ constexpr size_t kHeaderBytes = 256;                 // device error record
 // [header][tickets][cache rows][partials], each part 256-aligned
 static __device__ __align__(256) unsigned char g_attn_scratch[kScratchBytes];
 
-// Device addresses of g_attn_scratch, one per device, found once. In host
-// code the name g_attn_scratch is only a host-side stand-in for the symbol,
-// never a device address, so kernels receive the looked-up address instead.
-constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
-std::mutex g_scratch_mu;
-
+// Device address of g_attn_scratch on the current device. In host code the
+// name g_attn_scratch is only a host-side stand-in for the symbol, never a
+// device address, so kernels receive the looked-up address instead. It is
+// looked up on every call (a query of the runtime, no stream work): a device
+// reset reloads the array, possibly at another address, and a cached pointer
+// would then be stale. The first lookup on a device loads the array.
 qsa_status scratch_on_current_device(void** addr) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return QSA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return QSA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || p == nullptr) return QSA_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *addr = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || p == nullptr) return QSA_ERR_CUDA;
+  *addr = p;
   return QSA_OK;
 }
 

@@ -642,14 +642,25 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const float* 
       tie_m |= (uint32_t)(in && !whole && key[e] == T) << e;
     }
   }
-  // this CTA's counts in index order, then the CTAs before it in the cluster
+  // this CTA's counts in index order, then the CTAs before it in the cluster.
+  // Inside one CTA the packed (ties << 16 | selected) scan cannot overflow: a
+  // CTA holds at most 32 x 1024 keys and selects at most kTopK. Summed over
+  // the lower-ranked CTAs the ties can pass 65,535 (a row of 131,073 equal
+  // scores puts 65,536 in the first four CTAs of eight), so the cluster-level
+  // counts are kept in two separate words.
   uint32_t total;
   const uint32_t excl = block_excl_scan(((uint32_t)__popc(tie_m) << 16) | (uint32_t)__popc(sel_m), wsum, &total);
-  if (tid == 0) cnt[0] = total;
+  if (tid == 0) {
+    cnt[0] = total & 0xffffu;  // selected
+    cnt[1] = total >> 16;      // tied
+  }
   cluster_sync();
-  uint32_t before = 0;  // packed (ties << 16 | selected) of the lower-ranked CTAs
-  for (uint32_t k = 0; k < crank; ++k) before += ld_peer(peer_addr(cnt, k));
-  const uint32_t e_before = (before >> 16) + (excl >> 16), s_before = (before & 0xffffu) + (excl & 0xffffu);
+  uint32_t s_peer = 0, e_peer = 0;  // selected and tied counts of the lower-ranked CTAs
+  for (uint32_t k = 0; k < crank; ++k) {
+    s_peer += ld_peer(peer_addr(cnt, k));
+    e_peer += ld_peer(peer_addr(cnt + 1, k));
+  }
+  const uint32_t e_before = e_peer + (excl >> 16), s_before = s_peer + (excl & 0xffffu);
   uint32_t take = need > e_before ? min(need - e_before, (uint32_t)__popc(tie_m)) : 0u;
   uint32_t rest = tie_m;
   for (; take > 0; --take) rest &= rest - 1u;

@@ -237,9 +237,11 @@ qsa_status qsa_decode(const qsa_dims* dims, const void* q_idx, const void* kc, c
  * 16 MiB array in the library's own device image, which every GPU that loads
  * the library keeps until the process exits.
  * The call allocates nothing (no cudaMalloc, no cudaFree, no allocating
- * library routine). The first call on a device looks up that array's device
- * address (cudaGetSymbolAddress) with the device current, so make it before
- * any stream capture. Every call shares the one array per device and clears
+ * library routine). Every call looks up that array's device address
+ * (cudaGetSymbolAddress) on the current device, so it stays valid after a
+ * device reset, which reloads the array; the first call on a device also
+ * loads the array there, so make it before any stream capture. Every call
+ * shares the one array per device and clears
  * its counters at the start, so calls that overlap on the GPU (different
  * streams, or different host threads on one device) race: issue them in
  * order on one stream. The CTA count is lowered to fit the array; when even

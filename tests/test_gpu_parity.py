@@ -6,10 +6,13 @@ Tolerances (stated by the step's contract and restated here):
   * attention outputs: max-abs <= 1e-2 with BF16 KV, <= 3e-2 with FP8 KV
     (the oracle decodes the same E4M3 bytes and scales).
 Top-k is bit-exact when both sides start from the same FP32 score buffer, so
-its unit tests feed both sides seeded score buffers. End to end, the oracle
-recomputes everything from the generator's inputs; a row whose 512th and
+its unit tests feed both sides seeded score buffers. End to end, every row is
+chained stage by stage: the GPU's scores against the oracle's, the oracle's
+selection on the GPU's own scores against the GPU's selection (bit-exact),
+and the oracle's attention over the GPU's own selection against the GPU's
+output. The pure oracle chain is compared as well; a row whose 512th and
 513th oracle scores are closer than the score tolerance can legitimately
-select differently and is counted, not compared.
+select differently there and is counted.
 """
 
 import math
@@ -229,15 +232,13 @@ TOPK_CASES = [
 ]
 
 
-@pytest.mark.parametrize("batch", [2, 80])
-@pytest.mark.parametrize("kind,n", TOPK_CASES)
-def test_topk_bit_exact_on_shared_scores(qsa, kind, n, batch):
+def _topk_case(qsa, kind, n, batch):
     # requests of 2 queries: rows of n and shorter ragged rows. 160 rows take
-    # one CTA per row; 4 rows longer than the register path take the cluster
-    # path (several CTAs per row).
+    # one CTA per row; 2 or 4 rows longer than the register path take the
+    # cluster path (several CTAs per row).
     n_q = 2
     mb = max(n, 1)
-    lens = ([[n, max(0, n - 37)], [max(0, n // 3), n]] * (batch // 2))[:batch]
+    lens = ([[n, max(0, n - 37)], [max(0, n // 3), n]] * ((batch + 1) // 2))[:batch]
     # query k of a row with L full blocks sits at 4L + k - 1 (k partial tokens)
     q_pos = [[max(0, 4 * L + k - 1) for k, L in enumerate(row)] for row in lens]
     for row in q_pos:
@@ -260,6 +261,25 @@ def test_topk_bit_exact_on_shared_scores(qsa, kind, n, batch):
             ref_b = O.topk_blocks(scores[r, j, : O.n_full(p)])
             assert np.array_equal(gb[r, j], ref_b), (r, j)
             assert np.array_equal(gp[r, j], O.select_positions(ref_b, p)), (r, j)
+
+
+@pytest.mark.parametrize("batch", [2, 80])
+@pytest.mark.parametrize("kind,n", TOPK_CASES)
+def test_topk_bit_exact_on_shared_scores(qsa, kind, n, batch):
+    _topk_case(qsa, kind, n, batch)
+
+
+@pytest.mark.parametrize("batch", [1, 2])
+@pytest.mark.parametrize("n", [98305, 131073, 262144, 262145])
+@pytest.mark.parametrize("kind", ["all_equal", "two_values", "ties_at_threshold"])
+def test_topk_long_rows_with_many_ties_at_small_batches(qsa, kind, n, batch):
+    # 2 or 4 rows of up to 262,144 blocks take the cluster path with eight
+    # CTAs per row and up to 32 keys per thread; all-equal and two-valued rows
+    # put more than 65,535 tied blocks in the CTAs before the last ones, so the
+    # slots of the ties taken depend on the counts of every lower-ranked CTA.
+    # One block more (262,145) leaves the cluster path for the long-row path
+    # (radix passes over the whole row, listed 65,536 blocks at a time).
+    _topk_case(qsa, kind, n, batch)
 
 
 def test_topk_is_deterministic_across_runs(qsa):
@@ -385,9 +405,68 @@ def _flip_is_near_tie(gpu_blk, ref_blk, ref_scores, k=512, tol=SCORE_RTOL):
     return all(abs(float(ref_scores[b]) - thr) <= band for b in g ^ o)
 
 
+def _oracle_request(spec, g, r):
+    """The oracle's own view of request r, copied from the generator's
+    tensors (its pages renumbered 0..n-1), with its compressed keys."""
+    npg = spec.pages_per_request()[r]
+    pages = g["page_table"][r, :npg].long()
+    npi = {
+        "q_idx": bits(g["q_idx"][r : r + 1]),
+        "q": bits(g["q"][r : r + 1]),
+        "k_cache": bits(g["k_cache"][pages]),
+        "v_cache": bits(g["v_cache"][pages]),
+        "k_scale": g["k_scale"].cpu().numpy(),
+        "v_scale": g["v_scale"].cpu().numpy(),
+        "page_table": np.arange(npg, dtype=np.int32)[None],
+        "q_pos": bits(g["q_pos"][r : r + 1]),
+    }
+    npi["kc"] = O.compress_keys(bits(g["idx_keys"][r]), spec.max_blocks())[None]
+    return npi
+
+
+def _check_row_chain(spec, npi, j, got_scores, got_blk, got_pos, got_out):
+    """Stage-by-stage parity of one (request, query) row of a fused step:
+
+      1. the GPU's FP32 scores against the oracle's scores (1e-4 relative);
+      2. the oracle's top-k and selection run on the GPU's own FP32 scores
+         against the GPU's block ids and selection buffer, bit-exact;
+      3. the oracle's attention over the GPU's own selection buffer against
+         the GPU's output (1e-2 BF16 KV, 3e-2 FP8 KV);
+      4. the pure oracle chain (oracle scores -> oracle selection -> oracle
+         attention): the same selection and output, unless the two selections
+         differ only in blocks within the score tolerance of the oracle's 512th
+         score (FP32 rounding may move that boundary).
+
+    Returns True when the pure oracle chain took another boundary block."""
+    p = int(npi["q_pos"][0, j])
+    fp8 = spec.kv_dtype == "fp8"
+    ks, vs = (npi["k_scale"], npi["v_scale"]) if fp8 else (None, None)
+    res = O.decode_step(npi, spec.kv_dtype, rows=[(0, j)])
+    ref_s = res["scores"][(0, j)]
+    nb = ref_s.shape[0]
+    err = np.abs(got_scores[:nb].astype(np.float64) - ref_s) / np.maximum(np.abs(ref_s), 1.0)
+    assert np.max(err, initial=0.0) <= SCORE_RTOL, (j, "scores")
+    own_blk = O.topk_blocks(got_scores[:nb])
+    assert np.array_equal(got_blk, own_blk), (j, "selection on the GPU's scores")
+    assert np.array_equal(got_pos, O.select_positions(own_blk, p)), (j, "selection buffer")
+    own_out = O.sparse_attn(npi["q"][0, j], npi["k_cache"], npi["v_cache"], npi["page_table"][0], got_pos,
+                            spec.kv_dtype, ks, vs)
+    err = np.max(np.abs(got_out - own_out))
+    assert err <= ATOL[spec.kv_dtype], (j, "attention over the GPU's selection", err)
+    if not np.array_equal(got_blk, res["sel_blk"][(0, j)]):
+        assert _flip_is_near_tie(got_blk, res["sel_blk"][(0, j)], ref_s), (j, "pure chain")
+        return True
+    assert np.array_equal(got_pos, res["sel_pos"][(0, j)]), (j, "pure chain")
+    err = np.max(np.abs(got_out - res["out"][(0, j)]))
+    assert err <= ATOL[spec.kv_dtype], (j, "pure chain", err)
+    return False
+
+
 def _decode_and_compare(qsa, spec, rows=None, gpu_inputs=None):
-    """Run qsa_decode on the GPU and compare the requested (r, j) rows with
-    the oracle computed from the same generator inputs."""
+    """Run qsa_decode on the GPU and check the requested (r, j) rows against
+    the oracle stage by stage (_check_row_chain). Every row passes the chained
+    stages; returns (rows whose pure oracle chain took another boundary block,
+    rows checked)."""
     g = gpu_inputs if gpu_inputs is not None else _dev(synth.make_inputs(spec))
     d = qsa.dims_for_spec(spec)
     ws = qsa.make_workspace(d)
@@ -403,43 +482,16 @@ def _decode_and_compare(qsa, spec, rows=None, gpu_inputs=None):
     if rows is None:
         rows = [(r, j) for r in range(spec.batch) for j in range(spec.n_q)]
     skipped = 0
-    ks = g["k_scale"].cpu().numpy()
-    vs = g["v_scale"].cpu().numpy()
+    sc_h, sb_h, sp_h, out_h = scores.cpu().numpy(), sb.cpu().numpy(), sp.cpu().numpy(), out.float().cpu().numpy()
     for r in sorted(set(r for r, _ in rows)):
-        # the oracle's own view of request r, copied from the generator's tensors
-        npg = spec.pages_per_request()[r]
-        pages = g["page_table"][r, :npg].long()
-        npi = {
-            "q_idx": bits(g["q_idx"][r : r + 1]),
-            "q": bits(g["q"][r : r + 1]),
-            "k_cache": bits(g["k_cache"][pages]),
-            "v_cache": bits(g["v_cache"][pages]),
-            "k_scale": ks,
-            "v_scale": vs,
-            "page_table": np.arange(npg, dtype=np.int32)[None],
-            "q_pos": bits(g["q_pos"][r : r + 1]),
-        }
-        idx = bits(g["idx_keys"][r])
-        npi["kc"] = O.compress_keys(idx, spec.max_blocks())[None]
+        npi = _oracle_request(spec, g, r)
         nb_r = O.n_full(max(spec.q_pos()[r]))
         assert np.array_equal(bits(kc[r, :nb_r]), npi["kc"][0, :nb_r])
         for rr, j in rows:
-            if rr != r:
-                continue
-            res = O.decode_step(npi, spec.kv_dtype, rows=[(0, j)])
-            ref_s = res["scores"][(0, j)]
-            got_s = scores[r, j, : ref_s.shape[0]].cpu().numpy().astype(np.float64)
-            assert np.max(np.abs(got_s - ref_s) / np.maximum(np.abs(ref_s), 1.0)) <= SCORE_RTOL
-            gsel = sb[r, j].cpu().numpy()
-            if not np.array_equal(gsel, res["sel_blk"][(0, j)]):
-                # allowed only as a near-tie at the selection boundary; then
-                # the two outputs average different sets and are not compared
-                assert _flip_is_near_tie(gsel, res["sel_blk"][(0, j)], ref_s), (r, j)
-                skipped += 1
-                continue
-            assert np.array_equal(sp[r, j].cpu().numpy(), res["sel_pos"][(0, j)]), (r, j)
-            err = np.max(np.abs(out[r, j].float().cpu().numpy() - res["out"][(0, j)]))
-            assert err <= ATOL[spec.kv_dtype], (r, j, err)
+            if rr == r:
+                skipped += _check_row_chain(spec, npi, j, sc_h[r, j], sb_h[r, j], sp_h[r, j], out_h[r, j])
+    print(f"{spec.name}: {len(rows)} rows checked stage by stage; the pure oracle chain took another "
+          f"boundary block in {skipped}")
     return skipped, len(rows)
 
 
@@ -457,11 +509,11 @@ def test_decode_full_size_batch1_configs(qsa, config):
 
 
 @pytest.mark.parametrize("config", [2, 3])
-def test_decode_full_size_batch32_sampled_rows(qsa, config):
+def test_decode_full_size_batch32_every_row(qsa, config):
+    # all 128 (request, query) rows of the 50K-token verify batch
     spec = synth.spec_for(config)
-    rows = [(0, 0), (5, 1), (11, 2), (17, 3), (31, 0), (31, 3), (23, 2)]
-    skipped, n = _decode_and_compare(qsa, spec, rows=rows)
-    assert skipped <= 1
+    skipped, n = _decode_and_compare(qsa, spec)
+    assert n == 128 and skipped <= 2
 
 
 def test_decode_long_context_batch1_sampled(qsa):
@@ -607,7 +659,7 @@ def test_score_chunk_reports_a_bad_position(qsa):
 # --------------------------------------------------------------------------
 
 @pytest.mark.parametrize("page_size,h,kv", [(64, 1, "bf16"), (16, 4, "fp8"), (128, 2, "bf16")])
-def test_paged_compressed_keys_match_the_contiguous_path(qsa, page_size, h, kv):
+def test_paged_compressed_keys_match_the_contiguous_path_and_the_oracle(qsa, page_size, h, kv):
     spec = synth.Spec(f"paged-kc-{page_size}", 3, 4, [3001, 1498, 5000], h, kv, True, 91 + page_size,
                       page_size=page_size)
     inp = synth.make_inputs(spec)
@@ -636,18 +688,32 @@ def test_paged_compressed_keys_match_the_contiguous_path(qsa, page_size, h, kv):
         for j in range(4):
             n = O.n_full(spec.q_pos()[r][j])
             assert np.array_equal(sc_h[r, j, :n].view(np.uint32), scp_h[r, j, :n].view(np.uint32)), (r, j)
-    # the fused step: the same selection and output, bit for bit
+    # the fused step: the same scores, selection and output, bit for bit
     outs = []
     for paged in (False, True):
         out = torch.empty((B, 4, 16, 128), dtype=torch.bfloat16, device="cuda")
+        scs = torch.empty((B, 4, mb), device="cuda")
+        sb = torch.empty((B, 4, 512), dtype=torch.int32, device="cuda")
         sp = torch.empty((B, 4, 2051), dtype=torch.int32, device="cuda")
         fn = qsa.decode_paged if paged else qsa.decode
         fn(d, g["q_idx"], kcp if paged else kc, g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"],
-           g["page_table"], g["q_pos"], out, ws, sel_pos=sp)
+           g["page_table"], g["q_pos"], out, ws, scores=scs, sel_blk=sb, sel_pos=sp)
         _check_ok(qsa, ws)
-        outs.append((bits(out), sp.cpu().numpy()))
+        outs.append((bits(out), sp.cpu().numpy(), scs.cpu().numpy(), sb.cpu().numpy(), out.float().cpu().numpy()))
     assert np.array_equal(outs[0][1], outs[1][1])
     assert np.array_equal(outs[0][0], outs[1][0])
+    # and the paged path against the oracle: compressed keys bit-exact, then
+    # every row chained stage by stage (scores, selection, attention)
+    _, _, sc_p, sb_p, out_p = outs[1]
+    skipped = 0
+    for r in range(B):
+        npi = _oracle_request(spec, g, r)
+        nb = O.n_full(max(spec.q_pos()[r]))
+        b = np.arange(nb)
+        assert np.array_equal(kcp_h[pt[r, b // bpp], b % bpp], npi["kc"][0, :nb]), r
+        for j in range(4):
+            skipped += _check_row_chain(spec, npi, j, sc_p[r, j], sb_p[r, j], outs[1][1][r, j], out_p[r, j])
+    assert skipped <= 1
 
 
 # --------------------------------------------------------------------------
@@ -836,6 +902,48 @@ def test_fp8_every_code_through_attention(qsa):
         for hq in range(16):
             want = O.e4m3_to_f64(vh[page0, hq // 8, tok])
             assert np.array_equal(got[0, j, hq], want), (j, hq)
+
+
+@pytest.mark.parametrize("kv", ["fp8", "bf16"])
+@pytest.mark.parametrize("magnitude", [1e5, 1e-7])
+def test_queries_outside_fp16_range(qsa, kv, magnitude):
+    # The query is BF16 for either cache type. The FP8 path contracts in FP16,
+    # whose range BF16 exceeds (65,504 at the top, normal down to 6.1e-5), so
+    # queries near 1e5 (past FP16's largest value) and near 1e-7 (FP16
+    # subnormals) must still match the oracle. Tiny queries get a large
+    # softmax scale, so that their logits are of order one and every bit of
+    # the query matters; large ones make each head's softmax nearly one-hot.
+    spec = small_spec([4000, 2600], n_q=2, kv_dtype=kv, seed=71)
+    inp = synth.make_inputs(spec)
+    q = (inp["q"].float() * magnitude).to(torch.bfloat16)
+    q[1, 1, 8:] = inp["q"][1, 1, 8:]  # heads of another magnitude in the same call (KV group 1)
+    inp["q"] = q
+    npi = to_numpy_inputs(inp)
+    sm_scale = (1.0 / magnitude) / math.sqrt(128) if magnitude < 1 else 1.0 / math.sqrt(128)
+    d = qsa.dims_for_spec(spec)
+    d.sm_scale = sm_scale
+    ws = qsa.make_workspace(d)
+    g = _dev(inp)
+    rng = np.random.default_rng(72)
+    sel = np.full((2, 2, 2051), -1, np.int32)
+    for r in range(2):
+        for j in range(2):
+            p = spec.q_pos()[r][j]
+            sel[r, j] = np.sort(rng.choice(p + 1, 2051, replace=False))
+    out = torch.full((2, 2, 16, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    qsa.sparse_attn(d, g["q"], g["k_cache"], g["v_cache"], g["k_scale"], g["v_scale"], g["page_table"],
+                    torch.from_numpy(sel).cuda(), g["q_pos"], out, ws)
+    _check_ok(qsa, ws)
+    got = out.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    fp8 = kv == "fp8"
+    for r in range(2):
+        for j in range(2):
+            ref = O.sparse_attn(npi["q"][r, j], npi["k_cache"], npi["v_cache"], npi["page_table"][r], sel[r, j],
+                                kv, npi["k_scale"] if fp8 else None, npi["v_scale"] if fp8 else None,
+                                sm_scale=float(np.float32(sm_scale)))
+            err = np.max(np.abs(got[r, j] - ref))
+            assert err <= ATOL[kv], (r, j, err)
 
 
 def test_bf16_single_position_returns_its_v_row_exactly(qsa):
