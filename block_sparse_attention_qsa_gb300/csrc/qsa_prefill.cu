@@ -9,91 +9,138 @@
 // FP32 accumulation, each query keeping only its causal blocks
 // b < floor((p_i + 1) / 4).
 //
-// Design. One CTA per tile of 128 blocks x 64 queries of one request, 8
-// warps of 32 blocks x 32 queries on mma.sync m16n8k16. Each index head is
-// one 128-wide k stage: the tile's key rows and query rows are copied into
-// shared memory with cp.async (rows padded so ldmatrix is conflict-free),
-// the first while the tile's query positions are read, the next head's while
-// one head is multiplied. The FP32 tile goes back through shared memory so
-// that each query's scores are written as consecutive blocks. For a chunk of
-// 1,024 queries the scores written (4 bytes per query and block) are several
-// times the bytes read and about four times the tensor work's time at the
-// measured peaks: the kernel is bound by HBM writes, not by the tensor cores.
+// Design (Blackwell tensor cores). One CTA of 4 warps per tile of 128 blocks
+// x 128 queries of one request. For each index head, TMA copies the tile's
+// 128 compressed-key rows and 128 query rows (256 bytes each) into shared
+// memory in the 128-byte swizzled layout the tensor core reads, completing an
+// mbarrier; one thread issues tcgen05.mma (M = 128 blocks, N = 128 queries,
+// K = 16 per instruction) into an FP32 accumulator in tensor memory (TMEM:
+// lane = block, column = query), and tcgen05.commit signals the epilogue. Two
+// heads' stages are in flight when there are several heads. The epilogue
+// reads the accumulator back with tcgen05.ld: warp w owns TMEM lanes (blocks)
+// 32w..32w+31, so for every query a warp stores 32 consecutive scores (128
+// contiguous bytes) of that query's row, the causal ones only. Scores are
+// 4 bytes per (query, block) against 0.5 read, so the kernel is bound by the
+// score writes, not by the tensor cores.
+//
+// Every wait (mbarrier phases) is bounded by a clock limit; past it the kernel
+// records a timeout in the workspace header, issues nothing more, waits
+// (bounded again) for its own copies in flight, frees its TMEM and returns.
+#include <cuda.h>
+
 #include "qsa_internal.cuh"
 
 namespace qsa {
 namespace {
 
-constexpr int kBM = 128;            // blocks per tile (M)
-constexpr int kBN = 64;             // queries per tile (N)
-constexpr int kBK = 128;            // one index head's dims per k stage
-constexpr int kLd = kBK + 8;        // padded row, in BF16 elements (272 bytes)
-constexpr int kPThreads = 256;      // 8 warps: 4 along M x 2 along N
-constexpr int kStageElems = (kBM + kBN) * kLd;
-constexpr int kOutLd = kBM + 4;     // padded row of the FP32 output tile
+constexpr int kTM = 128;        // blocks per tile (MMA M, TMEM lanes)
+constexpr int kTN = 128;        // queries per tile (MMA N, TMEM columns)
+constexpr int kPThreads = 128;  // 4 warps: each reads 32 TMEM lanes in the epilogue
+constexpr int kHalfBytes = kTM * 128;      // one 64-dim half of a tile's rows: 128 rows x 128 B (16 KB)
+constexpr int kStageBytes = 4 * kHalfBytes;  // keys (2 halves) + queries (2 halves) of one index head
+constexpr uint32_t kTmemCols = kTN;        // FP32 accumulator columns
+constexpr long long kWaitCycles = 1LL << 31;  // about one second at 2 GHz
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-
-// 16-byte async copy; src_bytes 0 fills zeros
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
-               : "memory");
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-
-__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_addr(p)));
-}
-
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// waits for the phase with the given parity to complete; false after the clock limit
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return false;
+  return true;
 }
 
-__global__ void __launch_bounds__(kPThreads) score_chunk_kernel(const __nv_bfloat16* __restrict__ q_idx,
-                                                              const __nv_bfloat16* __restrict__ kc,
+// 3-D tiled TMA load of box (x, y, z) into shared memory, completing on bar
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzled layout (rows of 128 bytes, 8-row groups 1,024 bytes apart, the
+// layout TMA writes with 128-byte swizzling): start address >> 4 in bits
+// 0-13, leading-dimension offset (unused by this layout) 1 in bits 16-29,
+// stride between 8-row groups (1,024 >> 4) in bits 32-45, descriptor version
+// 1 in bits 46-47, swizzle mode 2 (128 bytes) in bits 61-63.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3fffu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: FP32 accumulator (bits
+// 4-5 = 1), BF16 A and B (bits 7-9 and 10-12 = 1), both K-major (bits 15, 16
+// = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTN >> 3) << 17) |
+                            ((uint32_t)(kTM >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16_tmem(uint32_t d_tmem, uint64_t a, uint64_t b, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(kIdesc), "r"((uint32_t)acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 32 consecutive FP32 accumulator columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__global__ void __launch_bounds__(kPThreads) score_chunk_kernel(const __grid_constant__ CUtensorMap tm_kc,
+                                                              const __grid_constant__ CUtensorMap tm_q,
                                                               const int32_t* __restrict__ q_pos,
                                                               float* __restrict__ scores, int32_t* err,
-                                                              int n_chunk, int H, int max_blocks) {
-  extern __shared__ __align__(16) __nv_bfloat16 psm[];
-  __shared__ int s_nf[kBN];  // causal blocks of each query of the tile (0 for none)
+                                                              int n_chunk, int H, int max_blocks, int stages) {
+  extern __shared__ uint8_t psm_raw[];
+  // stage buffers at a 1,024-byte boundary (the swizzle pattern repeats every 1,024 bytes)
+  uint8_t* psm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(psm_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full_bar[2], empty_bar[2], done_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_nf[kTN];  // causal blocks of each query of the tile (0 for none)
   __shared__ int s_nf_max;
+  __shared__ int s_timeout;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b0 = blockIdx.x * kBM, i0 = blockIdx.y * kBN, r = blockIdx.z;
+  const int b0 = blockIdx.x * kTM, i0 = blockIdx.y * kTN, r = blockIdx.z;
 
-  // stage h: the tile's 128 key rows and 64 query rows of index head h
-  auto stage = [&](int h, int buf) {
-    __nv_bfloat16* A = psm + buf * kStageElems;
-    __nv_bfloat16* B = A + kBM * kLd;
-    for (int c = tid; c < kBM * 16; c += kPThreads) {  // 16 chunks of 16 bytes per row
-      const int row = c >> 4, ch = c & 15;
-      const int b = b0 + row;
-      const bool ok = b < max_blocks;
-      const __nv_bfloat16* src = kc + (((size_t)r * max_blocks + (ok ? b : 0)) * H + h) * kBK + ch * 8;
-      cp_async16(A + row * kLd + ch * 8, src, ok ? 16 : 0);
-    }
-    for (int c = tid; c < kBN * 16; c += kPThreads) {
-      const int row = c >> 4, ch = c & 15;
-      const int i = i0 + row;
-      const bool ok = i < n_chunk;
-      const __nv_bfloat16* src = q_idx + (((size_t)r * n_chunk + (ok ? i : 0)) * H + h) * kBK + ch * 8;
-      cp_async16(B + row * kLd + ch * 8, src, ok ? 16 : 0);
-    }
-  };
-
-  // the tile's first head is copied while the queries' positions are read
-  stage(0, 0);
-  asm volatile("cp.async.commit_group;" ::: "memory");
-  if (tid == 0) s_nf_max = 0;
+  if (tid == 0) {
+    s_nf_max = 0;
+    s_timeout = 0;
+  }
   __syncthreads();
-  if (tid < kBN) {
-    const int i = i0 + tid;
+  {
+    const int i = i0 + tid;  // kPThreads == kTN: one query per thread
     int nf = 0;
     if (i < n_chunk) {
       const int p = q_pos[(size_t)r * n_chunk + i];
@@ -107,90 +154,162 @@ __global__ void __launch_bounds__(kPThreads) score_chunk_kernel(const __nv_bfloa
     atomicMax(&s_nf_max, nf);
   }
   __syncthreads();
-  if (b0 >= s_nf_max) {  // no query of the tile sees these blocks
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    return;
+  if (b0 >= s_nf_max) return;  // no query of the tile sees these blocks: nothing allocated or issued
+
+  // TMEM accumulator (one warp allocates) and the barriers (one thread)
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-
-  const int wm = warp & 3, wn = warp >> 2;  // this warp's 32 blocks x 32 queries
-  float acc[2][4][4];
-#pragma unroll
-  for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-    for (int ni = 0; ni < 4; ++ni) acc[mi][ni][0] = acc[mi][ni][1] = acc[mi][ni][2] = acc[mi][ni][3] = 0.f;
-
-  for (int h = 0; h < H; ++h) {
-    const int buf = h & 1;  // one stage buffer when H == 1
-    if (h + 1 < H) stage(h + 1, buf ^ 1);
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    asm volatile("cp.async.wait_group 1;" ::: "memory");  // stage h has landed
-    __syncthreads();
-    const __nv_bfloat16* A = psm + buf * kStageElems;
-    const __nv_bfloat16* B = A + kBM * kLd;
-#pragma unroll
-    for (int ks = 0; ks < kBK / 16; ++ks) {
-      uint32_t a[2][4], b[2][4];
-#pragma unroll
-      for (int mi = 0; mi < 2; ++mi)
-        ldmatrix_x4(a[mi], A + (wm * 32 + mi * 16 + (lane & 15)) * kLd + ks * 16 + (lane >> 4) * 8);
-      // two n8 tiles per ldmatrix.x4: (n rows, k 0-7), (n rows, k 8-15) of tiles 2j and 2j + 1
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-        ldmatrix_x4(b[j], B + (wn * 32 + j * 16 + (lane >> 4) * 8 + (lane & 7)) * kLd + ks * 16 +
-                              ((lane >> 3) & 1) * 8);
-#pragma unroll
-      for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          mma_bf16(acc[mi][2 * j], a[mi], b[j][0], b[j][1]);
-          mma_bf16(acc[mi][2 * j + 1], a[mi], b[j][2], b[j][3]);
-        }
+  if (tid == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
     }
-    __syncthreads();  // the stage is free for the copy two heads on
+    mbar_init(smem_u32(&done_bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-
-  // the FP32 tile, queries x blocks, through shared memory
-  float* T = reinterpret_cast<float*>(psm);
-  const int g = lane >> 2, c = lane & 3;
-#pragma unroll
-  for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-    for (int ni = 0; ni < 4; ++ni) {
-      const int m = wm * 32 + mi * 16 + g, n = wn * 32 + ni * 8 + 2 * c;
-      T[n * kOutLd + m] = acc[mi][ni][0];
-      T[(n + 1) * kOutLd + m] = acc[mi][ni][1];
-      T[n * kOutLd + m + 8] = acc[mi][ni][2];
-      T[(n + 1) * kOutLd + m + 8] = acc[mi][ni][3];
-    }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  // each warp writes whole query rows: 128 consecutive blocks, causal ones only
-  for (int n = warp; n < kBN; n += kPThreads / 32) {
-    const int i = i0 + n;
-    if (i >= n_chunk) break;
-    const int nf = s_nf[n];
-    float* dst = scores + ((size_t)r * n_chunk + i) * max_blocks + b0;
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = s_tmem;
+
+  if (tid == 0) {
+    // producer and MMA issuer
+    auto load_head = [&](int h, int s) {
+      const uint32_t base = smem_u32(psm + s * kStageBytes);
+      const uint32_t bar = smem_u32(&full_bar[s]);
+      mbar_expect_tx(bar, kStageBytes);
+      tma_load_3d(base, &tm_kc, h * 128, b0, r, bar);
+      tma_load_3d(base + kHalfBytes, &tm_kc, h * 128 + 64, b0, r, bar);
+      tma_load_3d(base + 2 * kHalfBytes, &tm_q, h * 128, i0, r, bar);
+      tma_load_3d(base + 3 * kHalfBytes, &tm_q, h * 128 + 64, i0, r, bar);
+    };
+    bool pending[2] = {false, false};  // a stage's copy issued and not yet seen complete
+    uint32_t pend_par[2] = {0u, 0u};    // the phase parity that copy completes
+    for (int h = 0; h < stages && h < H; ++h) {
+      load_head(h, h);
+      pending[h] = true;
+    }
+    bool ok = true;
+    for (int h = 0; h < H && ok; ++h) {
+      const int s = h % stages;
+      const uint32_t par = (uint32_t)(h / stages) & 1u;
+      if (!mbar_wait(smem_u32(&full_bar[s]), par)) {
+        ok = false;
+        break;
+      }
+      pending[s] = false;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t a0 = smem_u32(psm + s * kStageBytes), bq = a0 + 2 * kHalfBytes;
 #pragma unroll
-    for (int k = 0; k < kBM / 32; ++k) {
-      const int m = k * 32 + lane;
-      if (b0 + m < nf) dst[m] = T[n * kOutLd + m];
+      for (int k = 0; k < 8; ++k) {  // 16 dims per instruction: 4 steps of 32 bytes in each 64-dim half
+        const uint32_t off = (uint32_t)(k >> 2) * kHalfBytes + (uint32_t)(k & 3) * 32u;
+        mma_bf16_tmem(tmem, sw128_desc(a0 + off), sw128_desc(bq + off), h > 0 || k > 0);
+      }
+      if (h + stages < H) {
+        mma_commit(smem_u32(&empty_bar[s]));  // the stage is free once these MMAs have read it
+        if (!mbar_wait(smem_u32(&empty_bar[s]), par)) {
+          ok = false;
+          break;
+        }
+        load_head(h + stages, s);
+        pending[s] = true;
+        pend_par[s] = par ^ 1u;
+      }
+    }
+    if (!ok) {
+      s_timeout = 1;
+      record_error(err, kErrTimeout, r, i0, b0);
+      for (int s = 0; s < 2; ++s)  // copies still in flight land before the CTA leaves (bounded)
+        if (pending[s]) mbar_wait(smem_u32(&full_bar[s]), pend_par[s]);
+    }
+    mma_commit(smem_u32(&done_bar));  // arrives once every MMA issued above has completed
+  }
+  __syncwarp();
+
+  // epilogue: warp w reads TMEM lanes 32w..32w+31 (blocks b0 + 32w + lane)
+  const bool done = mbar_wait(smem_u32(&done_bar), 0);
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  if (!done && lane == 0) {
+    s_timeout = 1;
+    record_error(err, kErrTimeout, r, i0, b0);
+  }
+  __syncthreads();
+  if (!s_timeout) {
+    const int b = b0 + warp * 32 + lane;
+    float* dst = scores + (size_t)r * n_chunk * max_blocks + b;
+#pragma unroll 1
+    for (int c0 = 0; c0 < kTN; c0 += 32) {
+      if (i0 + c0 >= n_chunk) break;  // warp-uniform
+      float v[32];
+      __syncwarp();
+      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+      for (int n = 0; n < 32; ++n) {
+        const int i = i0 + c0 + n;
+        if (i < n_chunk && b < s_nf[c0 + n]) dst[(size_t)i * max_blocks] = v[n];
+      }
     }
   }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (the
+// library links no driver library directly)
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiled>(p);
+  }();
+  return fn;
+}
+
+// [B][rows][H * 128] BF16 as a 3-D tensor map with boxes of 64 dims x 128
+// rows x 1, swizzled by 128 bytes (rows past `rows` read as zeros)
+bool make_map(CUtensorMap* m, const __nv_bfloat16* base, int H, int rows, int B) {
+  const EncodeTiled enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)H * 128, (cuuint64_t)rows, (cuuint64_t)B};
+  const cuuint64_t strides[2] = {(cuuint64_t)H * 256, (cuuint64_t)rows * H * 256};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kTM, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
 
 cudaError_t launch_score_chunk(const qsa_dims& d, int n_chunk, const __nv_bfloat16* q_idx, const __nv_bfloat16* kc,
                                const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s) {
-  // two stage buffers only when there is a second index head to overlap with
-  // (one head: 52 KB per CTA, four CTAs per SM)
-  const size_t smem = (size_t)(d.n_idx_heads > 1 ? 2 : 1) * kStageElems * sizeof(__nv_bfloat16);
-  static_assert((size_t)kBN * kOutLd * sizeof(float) <= (size_t)kStageElems * sizeof(__nv_bfloat16),
-                "output tile larger than a stage buffer");
+  static_assert(kTM == kTN && kPThreads == kTN, "one query per thread when reading positions");
+  alignas(64) CUtensorMap tm_kc, tm_q;
+  if (!make_map(&tm_kc, kc, d.n_idx_heads, d.max_blocks, d.batch) ||
+      !make_map(&tm_q, q_idx, d.n_idx_heads, n_chunk, d.batch))
+    return cudaErrorInvalidValue;
+  // one stage when there is one index head (three CTAs per SM), else two
+  // (the next head's copy overlaps this head's MMAs)
+  const int stages = d.n_idx_heads > 1 ? 2 : 1;
+  const size_t smem = (size_t)stages * kStageBytes + 1024;
   static DeviceSlots smem_slots;
   if (const cudaError_t e = smem_slots.raise_smem(score_chunk_kernel, smem); e != cudaSuccess) return e;
-  const dim3 grid((d.max_blocks + kBM - 1) / kBM, (n_chunk + kBN - 1) / kBN, d.batch);
-  return launch_k(score_chunk_kernel, grid, dim3(kPThreads), smem, s, false, q_idx, kc, q_pos, scores, err, n_chunk,
-                  d.n_idx_heads, d.max_blocks);
+  const dim3 grid((d.max_blocks + kTM - 1) / kTM, (n_chunk + kTN - 1) / kTN, d.batch);
+  return launch_k(score_chunk_kernel, grid, dim3(kPThreads), smem, s, false, tm_kc, tm_q, q_pos, scores, err,
+                  n_chunk, d.n_idx_heads, d.max_blocks, stages);
 }
 
 }  // namespace qsa
