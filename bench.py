@@ -391,18 +391,30 @@ def run_draft(qsa, args, spec, st, sel_host, flush, stream, world, rank):
 
 def run_chunk(qsa, args, world, rank):
     """Chunked (prefill) scoring: args.chunk queries of one 50K-token request
-    at the chunk's last positions, against all of the request's blocks."""
+    at the chunk's last positions, against all of the request's blocks. The
+    block capacity of the buffers (max_blocks) is the request's 12,501 blocks
+    rounded up to a multiple of 32, so every score row starts on a 128-byte
+    boundary (the capacity is the caller's choice; unaligned rows cost the
+    stores partial sectors)."""
     spec = synth.spec_for(1)
     g = synth.make_inputs(spec, device="cuda")
+    d0 = qsa.dims_for_spec(spec)
+    ws0 = qsa.make_workspace(d0)
+    mb = spec.max_blocks()
+    kc0 = torch.zeros((1, mb, spec.n_idx_heads, spec.head_dim), dtype=torch.bfloat16, device="cuda")
+    qsa.compress_keys(d0, g["idx_keys"], g["q_pos"], kc0, ws0)
+    mb_pad = (mb + 31) // 32 * 32
     d = qsa.dims_for_spec(spec)
+    d.max_blocks = mb_pad
     ws = qsa.make_workspace(d)
-    kc = torch.zeros((1, spec.max_blocks(), spec.n_idx_heads, spec.head_dim), dtype=torch.bfloat16, device="cuda")
-    qsa.compress_keys(d, g["idx_keys"], g["q_pos"], kc, ws)
+    kc = torch.zeros((1, mb_pad, spec.n_idx_heads, spec.head_dim), dtype=torch.bfloat16, device="cuda")
+    kc[:, :mb] = kc0
+    del kc0, ws0
     n = args.chunk
     L = spec.first_pos[0]
     qi = synth.normal_bf16((1, n, spec.n_idx_heads, spec.head_dim), spec.seed + 77, device="cuda")
     qp = torch.tensor([[L - (n - 1 - i) for i in range(n)]], dtype=torch.int32, device="cuda")
-    sc = torch.empty((1, n, spec.max_blocks()), dtype=torch.float32, device="cuda")
+    sc = torch.empty((1, n, mb_pad), dtype=torch.float32, device="cuda")
     call = lambda: qsa.score_chunk(d, qi, kc, qp, sc, ws)
     call()
     status, info = qsa.check_errors(ws)
@@ -421,6 +433,7 @@ def run_chunk(qsa, args, world, rank):
     flops = 2 * sum(nf) * spec.n_idx_heads * spec.head_dim
     if rank == 0:
         print(json.dumps({"metric": "QSA chunked (prefill) scoring", "workload": f"b1-ctx{L}-chunk{n}",
+                          "max_blocks": mb_pad, "kernel": "tcgen05 (TMA, TMEM accumulators), persistent",
                           "latency_us": round(ms * 1e3, 2),
                           "latency_us_p10_p50_p90": [round(float(np.percentile(ms_list, q)) * 1e3, 2)
                                                      for q in (10, 50, 90)],

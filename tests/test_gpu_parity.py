@@ -595,28 +595,40 @@ def _run_decode(qsa, spec, g):
 # chunked (prefill) scoring: many queries per request (qsa_score_chunk)
 # --------------------------------------------------------------------------
 
-def _chunk_case(qsa, spec, n_chunk, q_pos, seed):
+def _chunk_case(qsa, spec, n_chunk, q_pos, seed, pad_to=1):
+    """Chunked scoring of n_chunk queries per request; the buffers' block
+    capacity is the spec's max_blocks rounded up to a multiple of pad_to."""
     inp = synth.make_inputs(spec)
     g = _dev(inp)
     d = qsa.dims_for_spec(spec)
     ws = qsa.make_workspace(d)
-    kc = torch.zeros((spec.batch, spec.max_blocks(), spec.n_idx_heads, 128), dtype=torch.bfloat16, device="cuda")
+    mb = spec.max_blocks()
+    kc = torch.zeros((spec.batch, mb, spec.n_idx_heads, 128), dtype=torch.bfloat16, device="cuda")
     qsa.compress_keys(d, g["idx_keys"], g["q_pos"], kc, ws)
+    mb_pad = (mb + pad_to - 1) // pad_to * pad_to
+    if mb_pad != mb:
+        kcp = torch.zeros((spec.batch, mb_pad, spec.n_idx_heads, 128), dtype=torch.bfloat16, device="cuda")
+        kcp[:, :mb] = kc
+        kc = kcp
+        d.max_blocks = mb_pad
+        ws = qsa.make_workspace(d)
     qi = synth.normal_bf16((spec.batch, n_chunk, spec.n_idx_heads, 128), seed, device="cuda")
     qp = torch.tensor(q_pos, dtype=torch.int32, device="cuda")
-    sc = torch.full((spec.batch, n_chunk, spec.max_blocks()), float("nan"), device="cuda")
+    sc = torch.full((spec.batch, n_chunk, mb_pad), float("nan"), device="cuda")
     qsa.score_chunk(d, qi, kc, qp, sc, ws)
     return sc.cpu().numpy(), bits(qi), bits(kc), ws
 
 
-@pytest.mark.parametrize("h", [1, 2, 4])
-def test_score_chunk_parity(qsa, h):
+@pytest.mark.parametrize("h,pad_to", [(1, 1), (2, 1), (4, 1), (1, 32), (3, 32)])
+def test_score_chunk_parity(qsa, h, pad_to):
+    # two requests, 150 queries each: two 128-query tiles, the second ragged;
+    # block capacity as drawn (misaligned rows) or padded to 32 blocks
     spec = small_spec([5003, 2900], n_q=1, n_idx_heads=h, seed=31 + h)
-    n_chunk = 150  # three query tiles, the last ragged
+    n_chunk = 150
     q_pos = [[max(0, spec.first_pos[r] - 3 * (n_chunk - 1 - i)) for i in range(n_chunk)] for r in range(2)]
     q_pos[1][0] = 5  # a query with no full block yet... and one with 1
     q_pos[1][1] = 4
-    sc, qi, kcb, ws = _chunk_case(qsa, spec, n_chunk, q_pos, 9001 + h)
+    sc, qi, kcb, ws = _chunk_case(qsa, spec, n_chunk, q_pos, 9001 + h, pad_to)
     _check_ok(qsa, ws)
     for r in range(2):
         for i in range(n_chunk):
@@ -628,18 +640,22 @@ def test_score_chunk_parity(qsa, h):
             assert np.all(np.isnan(sc[r, i, n:])), (r, i)  # nothing written past the causal blocks
 
 
-def test_score_chunk_full_size_sampled(qsa):
-    spec = synth.spec_for(1)  # one request, 50,000-token context
+@pytest.mark.parametrize("pad_to", [1, 32])
+def test_score_chunk_full_size_sampled(qsa, pad_to):
+    # the benchmark's launch: one request of 50,000 tokens, 1,024 queries, block
+    # capacity padded to 32 blocks (aligned score rows); and unpadded
+    spec = synth.spec_for(1)
     n_chunk = 1024
     L = spec.first_pos[0]
     q_pos = [[L - (n_chunk - 1 - i) for i in range(n_chunk)]]
-    sc, qi, kcb, ws = _chunk_case(qsa, spec, n_chunk, q_pos, 9100)
+    sc, qi, kcb, ws = _chunk_case(qsa, spec, n_chunk, q_pos, 9100, pad_to)
     _check_ok(qsa, ws)
-    for i in (0, 1, 63, 64, 511, 777, 1023):
+    for i in (0, 1, 63, 64, 127, 128, 511, 777, 1000, 1023):
         p = q_pos[0][i]
         n = O.n_full(p)
         ref = O.score_row(qi[0, i], kcb[0], p)
         assert np.all(np.abs(sc[0, i, :n] - ref) <= SCORE_RTOL * np.maximum(np.abs(ref), 1.0)), i
+        assert np.all(np.isnan(sc[0, i, n:])), i
 
 
 def test_score_chunk_reports_a_bad_position(qsa):
