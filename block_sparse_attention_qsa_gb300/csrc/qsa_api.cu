@@ -38,8 +38,6 @@ WsLayout ws_layout(const qsa_dims& d, int num_sms) {
   off = align_up(off + rows * d.max_blocks * sizeof(float), 256);
   w.sel_row = off;
   off = align_up(off + rows * kDraftWidth * sizeof(int32_t), 256);
-  w.hist = off;
-  off = align_up(off + rows * kHistBins * sizeof(uint32_t), 256);
   w.total = off;
   return w;
 }
@@ -308,15 +306,13 @@ qsa_status decode_impl(const qsa_dims* dims, const void* q_idx, const void* kc, 
   if ((st = check_ws(dims, ws, ws_bytes, &w)) != QSA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* sc = scores ? scores : at<float>(ws, w.scores);
-  // the score kernel also counts each row's first radix digit for the selector
-  uint32_t* hist = at<uint32_t>(ws, w.hist);
   cudaError_t e = launch_score(*dims, static_cast<const __nv_bfloat16*>(q_idx),
                                static_cast<const __nv_bfloat16*>(kc), q_pos, sc, err_word(ws), s, false,
-                               kc_paged ? page_table : nullptr, hist);
+                               kc_paged ? page_table : nullptr);
   if (e != cudaSuccess) return QSA_ERR_CUDA;
   int32_t* srow = at<int32_t>(ws, w.sel_row);
   // block ids and positions only when the caller asked for them; attention needs the cache rows
-  e = launch_topk(*dims, sc, q_pos, sel_blk, sel_pos, err_word(ws), page_table, srow, s, true, hist);
+  e = launch_topk(*dims, sc, q_pos, sel_blk, sel_pos, err_word(ws), page_table, srow, s, true);
   if (e != cudaSuccess) return QSA_ERR_CUDA;
   const AttnPlan pl{w.units, w.tiles, w.grid};
   e = launch_attn(*dims, q, k_cache, v_cache, k_scale, v_scale, srow, out, at<int32_t>(ws, w.tickets),

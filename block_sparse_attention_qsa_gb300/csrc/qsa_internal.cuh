@@ -38,14 +38,11 @@ constexpr int kDraftWidth = kWidth + kMaxDraftGap;
 //   scores (decode)    float [B][n_q][max_blocks]
 //   sel_row            int32 [B][n_q][2051 + kMaxDraftGap]  cache row (KV head 0) of each
 //                      selected position (row stride 2051, or 2051 + kMaxDraftGap for draft steps)
-//   hist (decode)      uint32 [B][n_q][2048]   each row's histogram of the first radix digit
-//                      (top 11 key bits of its scores), counted by the score kernel and
-//                      consumed (then zeroed) by the selector
 // ---------------------------------------------------------------------------
 constexpr int kPartFloats = 2 * kGroup + kGroup * kDim;  // m[8], l[8], acc[8][128]
 
 struct WsLayout {
-  size_t tickets, partials, scores, sel_row, hist, total;
+  size_t tickets, partials, scores, sel_row, total;
   int units, tiles, grid;
 };
 
@@ -163,18 +160,14 @@ struct KcPages {
 cudaError_t launch_compress(const qsa_dims& d, const __nv_bfloat16* idx_keys, const int32_t* q_pos,
                             const int32_t* block_lo, __nv_bfloat16* kc, int32_t* err,
                             cudaStream_t s, const int32_t* page_table = nullptr);
-// hist (optional, inside qsa_decode): also count each row's first radix digit
-// ([B * n_q][2048], zero on entry) for the selector
 cudaError_t launch_score(const qsa_dims& d, const __nv_bfloat16* q_idx, const __nv_bfloat16* kc,
                          const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s, bool pdl,
-                         const int32_t* page_table = nullptr, uint32_t* hist = nullptr);
+                         const int32_t* page_table = nullptr);
 // page_table / sel_row (optional, inside qsa_decode): also write each selected
-// position's cache row for KV head 0, so attention skips the page lookup;
-// hist (optional): the rows' first-digit histograms counted by the score
-// kernel, used instead of a first counting pass and zeroed afterwards
+// position's cache row for KV head 0, so attention skips the page lookup
 cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q_pos,
                         int32_t* sel_blk, int32_t* sel_pos, int32_t* err, const int32_t* page_table,
-                        int32_t* sel_row, cudaStream_t s, bool pdl, uint32_t* hist = nullptr);
+                        int32_t* sel_row, cudaStream_t s, bool pdl);
 // many queries per request (a prefill chunk) against the request's blocks
 cudaError_t launch_score_chunk(const qsa_dims& d, int n_chunk, const __nv_bfloat16* q_idx, const __nv_bfloat16* kc,
                                const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s);

@@ -138,27 +138,17 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// First-digit histograms kept in shared memory per CTA: the requests its
-// warps start on, kHistSlots of them (a CTA's range of units rarely spans
-// more); the counts of other requests go straight to global memory.
-constexpr int kHistSlots = 2;
-
 template <int H, bool PAGED>
 __global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(const __nv_bfloat16* __restrict__ q_idx,
                                                     const uint4* __restrict__ kc,
                                                     const int32_t* __restrict__ q_pos,
                                                     float* __restrict__ scores, int32_t* err,
-                                                    int B, int n_q, int max_blocks, const KcPages kp,
-                                                    uint32_t* __restrict__ ghist) {
+                                                    int B, int n_q, int max_blocks, const KcPages kp) {
   using Geo = ScoreGeom<H>;
   constexpr int STEPS = Geo::STEPS, PD = Geo::PD;
   constexpr int CPB = H * 16;  // 16-B chunks per block row
-  // with ghist: [kHistSlots][n_q][kHistBins] first-digit counts of the CTA's first requests
-  extern __shared__ __align__(16) uint32_t s_dyn[];
-  uint32_t* s_hist = s_dyn;
-  int* s_off = reinterpret_cast<int*>(s_dyn + (ghist ? kHistSlots * n_q * kHistBins : 0));  // [B + 1] first unit (16 blocks) of each request
+  extern __shared__ int s_off[];  // [B + 1] first unit (16 blocks) of each request
   int* s_nb = s_off + B + 1;      // [B] full blocks of each request (its longest query)
-  __shared__ int s_r0;            // request of the CTA's first unit
 
   pdl_wait();  // no-op unless launched as a dependent
   // Let the selector launch now: its CTAs take each SM as this kernel's CTA
@@ -198,8 +188,6 @@ __global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(cons
       carry += __shfl_sync(kFull, v, 31);
     }
     if (lane == 0) s_off[B] = carry;
-  } else if (ghist) {
-    for (int i = threadIdx.x - 32; i < kHistSlots * n_q * kHistBins; i += blockDim.x - 32) s_hist[i] = 0;
   }
   __syncthreads();
 
@@ -216,16 +204,6 @@ __global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(cons
   }
   int r = lo;
   const int g = lane >> 2, c = lane & 3;
-  if (threadIdx.x == 0) s_r0 = r;  // warp 0's first unit is the CTA's first
-  if (ghist) __syncthreads();
-  const int r0 = s_r0;
-  // one score's first-digit count: the CTA's histogram of its request, or global memory
-  auto count = [&](int rr, int j, float v) {
-    const uint32_t bin = order_key(v) >> 21;
-    const int slot = rr - r0;
-    if (slot < kHistSlots) atomicAdd(&s_hist[(slot * n_q + j) * kHistBins + bin], 1u);
-    else atomicAdd(&ghist[((size_t)rr * n_q + j) * kHistBins + bin], 1u);
-  };
 
   while (u < u_end) {
     while (s_off[r + 1] <= u) ++r;
@@ -323,25 +301,10 @@ __global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(cons
           if (b < nb1) s1[b] = acc[1];
           if (b + 8 < nb0) s0[b + 8] = acc[2];
           if (b + 8 < nb1) s1[b + 8] = acc[3];
-          if (ghist) {
-            if (b < nb0) count(r, 2 * c, acc[0]);
-            if (b < nb1) count(r, 2 * c + 1, acc[1]);
-            if (b + 8 < nb0) count(r, 2 * c, acc[2]);
-            if (b + 8 < nb1) count(r, 2 * c + 1, acc[3]);
-          }
         }
       }
     }
     u = seg_end;  // the unrolled loop may step past the end of this request's units
-  }
-  if (ghist) {
-    // the CTA's counts, one global atomic per non-empty bin
-    __syncthreads();
-    for (int i = threadIdx.x; i < kHistSlots * n_q * kHistBins; i += blockDim.x) {
-      const uint32_t v = s_hist[i];
-      const int rr = r0 + i / (n_q * kHistBins);
-      if (v && rr < B) atomicAdd(&ghist[(size_t)rr * n_q * kHistBins + i % (n_q * kHistBins)], v);
-    }
   }
 }
 
@@ -363,10 +326,9 @@ KcPages kc_pages(const qsa_dims& d, const int32_t* page_table) {
 template <int H, bool PAGED>
 cudaError_t launch_score_h(const qsa_dims& d, const __nv_bfloat16* q_idx, const __nv_bfloat16* kc,
                            const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s,
-                           bool pdl, const KcPages& kp, uint32_t* hist) {
+                           bool pdl, const KcPages& kp) {
   auto kern = score_kernel<H, PAGED>;
-  const size_t smem = (size_t)(2 * d.batch + 1) * sizeof(int) +
-                      (hist ? (size_t)kHistSlots * d.n_q * kHistBins * sizeof(uint32_t) : 0);
+  const size_t smem = (size_t)(2 * d.batch + 1) * sizeof(int);
   static DeviceSlots occ_slots, smem_slots;  // one pair per instantiation
   const cudaError_t e = smem_slots.raise_smem(kern, smem);
   if (e != cudaSuccess) return e;
@@ -383,7 +345,7 @@ cudaError_t launch_score_h(const qsa_dims& d, const __nv_bfloat16* q_idx, const 
   if (want < warps) warps = want;
   const int grid = (int)((warps + 7) / 8 > 0 ? (warps + 7) / 8 : 1);
   return launch_k(kern, dim3(grid), dim3(256), smem, s, pdl, q_idx, reinterpret_cast<const uint4*>(kc), q_pos,
-                  scores, err, d.batch, d.n_q, d.max_blocks, kp, hist);
+                  scores, err, d.batch, d.n_q, d.max_blocks, kp);
 }
 
 }  // namespace
@@ -403,21 +365,21 @@ cudaError_t launch_compress(const qsa_dims& d, const __nv_bfloat16* idx_keys, co
 
 cudaError_t launch_score(const qsa_dims& d, const __nv_bfloat16* q_idx, const __nv_bfloat16* kc,
                          const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s,
-                         bool pdl, const int32_t* page_table, uint32_t* hist) {
+                         bool pdl, const int32_t* page_table) {
   const KcPages kp = kc_pages(d, page_table);
   if (page_table) {
     switch (d.n_idx_heads) {
-      case 1: return launch_score_h<1, true>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp, hist);
-      case 2: return launch_score_h<2, true>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp, hist);
-      case 3: return launch_score_h<3, true>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp, hist);
-      default: return launch_score_h<4, true>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp, hist);
+      case 1: return launch_score_h<1, true>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp);
+      case 2: return launch_score_h<2, true>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp);
+      case 3: return launch_score_h<3, true>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp);
+      default: return launch_score_h<4, true>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp);
     }
   }
   switch (d.n_idx_heads) {
-    case 1: return launch_score_h<1, false>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp, hist);
-    case 2: return launch_score_h<2, false>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp, hist);
-    case 3: return launch_score_h<3, false>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp, hist);
-    default: return launch_score_h<4, false>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp, hist);
+    case 1: return launch_score_h<1, false>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp);
+    case 2: return launch_score_h<2, false>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp);
+    case 3: return launch_score_h<3, false>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp);
+    default: return launch_score_h<4, false>(d, q_idx, kc, q_pos, scores, err, s, pdl, kp);
   }
 }
 

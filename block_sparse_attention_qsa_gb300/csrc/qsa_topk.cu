@@ -157,8 +157,7 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, bool valid, uint32_t bi
 // in blk. Starts after a barrier (zeroed histograms); ends with one.
 template <int KPT>
 __device__ __forceinline__ void select_regs(const float* srow, int n, int off, bool vec, uint32_t* hist,
-                                            uint32_t* hist2, uint32_t* wsum, int* res, int32_t* blk,
-                                            bool counted) {
+                                            uint32_t* hist2, uint32_t* wsum, int* res, int32_t* blk) {
   const int tid = threadIdx.x;
   const int span = n + off;
   const int v0 = tid * KPT;
@@ -186,9 +185,7 @@ __device__ __forceinline__ void select_regs(const float* srow, int n, int off, b
     key[4 * q + 2] = order_key(f.z);
     key[4 * q + 3] = order_key(f.w);
   }
-  // (the first digit's histogram is already in `hist` when the score kernel counted it)
-  if (counted) {
-  } else if (valid_m == kAll) {
+  if (valid_m == kAll) {
 #pragma unroll
     for (int e = 0; e < KPT; ++e) atomicAdd(&hist[key[e] >> 21], 1u);
   } else if (valid_m) {
@@ -276,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
                                                            int32_t* __restrict__ sel_pos,
                                                            int32_t* err, const RowOut ro, int rows,
                                                            int n_q, int max_blocks, int fast_cap,
-                                                           int key_cap, bool vec, uint32_t* ghist) {
+                                                           int key_cap, bool vec) {
   extern __shared__ __align__(16) uint32_t sm[];
   uint32_t* hist = sm;                                // [2048] digits 1 and 3
   uint32_t* hist2 = hist + 2048;                      // [2048] digit 2
@@ -322,16 +319,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
     const int r = row / n_q, j = row - r * n_q;
     const bool p_ok = p >= 0 && n_full_of(p) <= max_blocks && (!orow || (p >> ro.page_shift) < ro.max_pages);
     const int n = p_ok ? n_full_of(p) : 0;
-    // the row's first-digit counts from the score kernel: taken by the register
-    // path, and zeroed in every case for the next step
-    uint32_t* gh = ghist ? ghist + (size_t)row * kHistBins : nullptr;
-    const bool counted = gh && p_ok && n > kTopK && n <= fast_cap;
-    if (gh) {
-      for (int i = tid; i < kHistBins; i += kThreads) {
-        if (counted) hist[i] = gh[i];
-        gh[i] = 0;
-      }
-    }
     if (!p_ok || n <= kTopK) {
       if (!p_ok && tid == 0) record_error(err, kErrQueryPos, r, j, p);
       // every full block is kept (positions 0..p), or nothing for a bad position
@@ -351,12 +338,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
       // ---- register path ----
       const int off = vec ? (int)(((size_t)row * max_blocks) & 3) : 0;
       const int span = n + off;
-      if (span <= 4 * kThreads) select_regs<4>(srow, n, off, vec, hist, hist2, wsum, res, blk, counted);
-      else if (span <= 8 * kThreads) select_regs<8>(srow, n, off, vec, hist, hist2, wsum, res, blk, counted);
-      else if (span <= 12 * kThreads) select_regs<12>(srow, n, off, vec, hist, hist2, wsum, res, blk, counted);
-      else if (span <= 16 * kThreads) select_regs<16>(srow, n, off, vec, hist, hist2, wsum, res, blk, counted);
-      else if (span <= 20 * kThreads) select_regs<20>(srow, n, off, vec, hist, hist2, wsum, res, blk, counted);
-      else select_regs<24>(srow, n, off, vec, hist, hist2, wsum, res, blk, counted);
+      if (span <= 4 * kThreads) select_regs<4>(srow, n, off, vec, hist, hist2, wsum, res, blk);
+      else if (span <= 8 * kThreads) select_regs<8>(srow, n, off, vec, hist, hist2, wsum, res, blk);
+      else if (span <= 12 * kThreads) select_regs<12>(srow, n, off, vec, hist, hist2, wsum, res, blk);
+      else if (span <= 16 * kThreads) select_regs<16>(srow, n, off, vec, hist, hist2, wsum, res, blk);
+      else if (span <= 20 * kThreads) select_regs<20>(srow, n, off, vec, hist, hist2, wsum, res, blk);
+      else select_regs<24>(srow, n, off, vec, hist, hist2, wsum, res, blk);
     } else {
       // ---- long rows: radix passes over the whole row ----
       const bool in_smem = n <= key_cap;  // keys cached in shared memory
@@ -524,8 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const float* 
                                                                    const int32_t* __restrict__ q_pos,
                                                                    int32_t* __restrict__ sel_blk,
                                                                    int32_t* __restrict__ sel_pos, int32_t* err,
-                                                                   const RowOut ro, int n_q, int max_blocks,
-                                                                   uint32_t* ghist) {
+                                                                   const RowOut ro, int n_q, int max_blocks) {
   extern __shared__ __align__(16) uint32_t sm[];
   uint32_t* hist = sm;             // [2048] this CTA's digit-1 (then digit-3) counts
   uint32_t* hist2 = hist + 2048;   // [2048] this CTA's digit-2 counts
@@ -560,13 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const float* 
   const int32_t* pt = pt_ok ? pt_s : nullptr;
   const bool p_ok = p >= 0 && n_full_of(p) <= max_blocks && (!orow || (p >> ro.page_shift) < ro.max_pages);
   const int n = p_ok ? n_full_of(p) : 0;
-  // the row's first-digit counts from the score kernel, summed over the whole
-  // row: every CTA of the cluster reads them (instead of counting and summing
-  // its own), and CTA 0 zeroes them once all have (after the last barrier)
-  uint32_t* gh = ghist ? ghist + (size_t)row * kHistBins : nullptr;
   if (!p_ok || n <= kTopK) {
-    if (crank == 0 && gh)
-      for (int i = tid; i < kHistBins; i += kThreads) gh[i] = 0;
     if (crank == 0) {
       if (!p_ok && tid == 0) record_error(err, kErrQueryPos, r, j, p);
       if (ob)
@@ -598,20 +578,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const float* 
   };
 
   // pass 1: keys into registers, this CTA's histogram of the top 11 bits
-  // (or the row's, counted by the score kernel)
   uint32_t key[KPT];
 #pragma unroll
   for (int e = 0; e < KPT; ++e) key[e] = ((valid_m >> e) & 1u) ? order_key(srow[v0 + e]) : 0u;
-  if (gh) {
-    for (int i = tid; i < kHistBins; i += kThreads) gsum[i] = gh[i];
-    __syncthreads();
-  } else {
 #pragma unroll
-    for (int e = 0; e < KPT; ++e)
-      if ((valid_m >> e) & 1u) atomicAdd(&hist[key[e] >> 21], 1u);
-    cluster_sync();
-    cluster_sum(hist, 2048);
-  }
+  for (int e = 0; e < KPT; ++e)
+    if ((valid_m >> e) & 1u) atomicAdd(&hist[key[e] >> 21], 1u);
+  cluster_sync();
+  cluster_sum(hist, 2048);
   uint32_t need = kTopK;
   find_bin<2048>(gsum, need, wsum, res);
   const uint32_t d1 = (uint32_t)res[0];
@@ -714,14 +688,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const float* 
     if (orow) orow[kBlock * kTopK + tid] = pos < 0 ? -1 : row_of(ro, pt, r, pos, err, j);
   }
   cluster_sync();  // no CTA leaves while another may still read its counts
-  if (crank == 0 && gh)
-    for (int i = tid; i < kHistBins; i += kThreads) gh[i] = 0;
 }
 
 template <int KPT>
 cudaError_t launch_topk_cluster(int C, int rows, const float* scores, const int32_t* q_pos, int32_t* sel_blk,
                                 int32_t* sel_pos, int32_t* err, const RowOut& ro, int n_q, int max_blocks,
-                                cudaStream_t s, bool pdl, uint32_t* ghist) {
+                                cudaStream_t s, bool pdl) {
   const size_t smem = (size_t)kClHdrWords * sizeof(uint32_t);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(rows * C);
@@ -738,14 +710,14 @@ cudaError_t launch_topk_cluster(int C, int rows, const float* scores, const int3
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<KPT>, scores, q_pos, sel_blk, sel_pos, err, ro, n_q,
-                            max_blocks, ghist);
+                            max_blocks);
 }
 
 }  // namespace
 
 cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q_pos,
                         int32_t* sel_blk, int32_t* sel_pos, int32_t* err, const int32_t* page_table,
-                        int32_t* sel_row, cudaStream_t s, bool pdl, uint32_t* ghist) {
+                        int32_t* sel_row, cudaStream_t s, bool pdl) {
   const int rows = d.batch * d.n_q;
   // shared memory: the header, and the long-row path's keys (the register
   // path keeps its keys in registers)
@@ -789,19 +761,19 @@ cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q
     const int per_thread = ((mb + C - 1) / C + kThreads - 1) / kThreads;
     cudaError_t e = cudaErrorNotSupported;
     if (per_thread <= 4)
-      e = launch_topk_cluster<4>(C, rows, scores, q_pos, sel_blk, sel_pos, err, ro, d.n_q, mb, s, pdl, ghist);
+      e = launch_topk_cluster<4>(C, rows, scores, q_pos, sel_blk, sel_pos, err, ro, d.n_q, mb, s, pdl);
     else if (per_thread <= 8)
-      e = launch_topk_cluster<8>(C, rows, scores, q_pos, sel_blk, sel_pos, err, ro, d.n_q, mb, s, pdl, ghist);
+      e = launch_topk_cluster<8>(C, rows, scores, q_pos, sel_blk, sel_pos, err, ro, d.n_q, mb, s, pdl);
     else if (per_thread <= 16)
-      e = launch_topk_cluster<16>(C, rows, scores, q_pos, sel_blk, sel_pos, err, ro, d.n_q, mb, s, pdl, ghist);
+      e = launch_topk_cluster<16>(C, rows, scores, q_pos, sel_blk, sel_pos, err, ro, d.n_q, mb, s, pdl);
     else if (per_thread <= 32)
-      e = launch_topk_cluster<32>(C, rows, scores, q_pos, sel_blk, sel_pos, err, ro, d.n_q, mb, s, pdl, ghist);
+      e = launch_topk_cluster<32>(C, rows, scores, q_pos, sel_blk, sel_pos, err, ro, d.n_q, mb, s, pdl);
     if (e == cudaSuccess) return e;
     cudaGetLastError();  // a cluster the device cannot place: one CTA per row below
   }
   return launch_k(topk_kernel, dim3(grid), dim3(kThreads), smem, s, pdl, scores, q_pos, sel_blk,
                   sel_pos, err, ro, rows, d.n_q, d.max_blocks, fast_cap, key_cap,
-                  (reinterpret_cast<uintptr_t>(scores) & 15u) == 0, ghist);
+                  (reinterpret_cast<uintptr_t>(scores) & 15u) == 0);
 }
 
 }  // namespace qsa
