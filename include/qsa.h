@@ -263,7 +263,14 @@ qsa_status qsa_sparse_attn_noalloc(const qsa_dims* dims, const void* q, const vo
  * [B][n_chunk][max_blocks] FP32: scores[r][i][b] = sum_h sum_d
  * q_idx[r][i][h][d] * kc[r][b][h][d] in FP32 for b < (q_pos[r][i] + 1) / 4;
  * other entries are not written. 1 <= n_chunk <= QSA_MAX_CHUNK and batch <=
- * 65,535, else QSA_ERR_INVALID_ARG / QSA_ERR_UNSUPPORTED before any launch. */
+ * 65,535, else QSA_ERR_INVALID_ARG / QSA_ERR_UNSUPPORTED before any launch.
+ * Runs on the tensor cores through TMA tensor maps of q_idx and kc (built on
+ * the host each call; both 16-byte aligned, as checked). A max_blocks that is
+ * a multiple of 32 makes every score row start on a 128-byte boundary, which
+ * the kernel's row stores are fastest with (max_blocks is the buffers' block
+ * capacity, so padding it costs only memory). The kernel's waits between its
+ * own warps are bounded: one that gives up is reported as QSA_ERR_TIMEOUT by
+ * qsa_check_errors (kind 5), with that call's scores incomplete. */
 qsa_status qsa_score_chunk(const qsa_dims* dims, int32_t n_chunk, const void* q_idx, const void* kc,
                            const int32_t* q_pos, float* scores, void* ws, size_t ws_bytes, void* stream);
 
@@ -314,8 +321,8 @@ qsa_status qsa_draft_attn(const qsa_dims* dims, const void* q, const void* k_cac
  * Returns QSA_OK if no device-side error was recorded since the last check,
  * else QSA_ERR_BAD_INDEX (or QSA_ERR_TIMEOUT). `info` (may be NULL) receives
  * 4 int32: error kind (1 query position, 2 page id, 3 selected position,
- * 4 draft query not after its reused selection), request, query, offending
- * value. */
+ * 4 draft query not after its reused selection, 5 a bounded wait inside the
+ * chunked-scoring kernel gave up), request, query, offending value. */
 qsa_status qsa_check_errors(void* ws, void* stream, int32_t* info);
 
 #ifdef __cplusplus
