@@ -443,6 +443,15 @@ def run_chunk(qsa, args, world, rank):
                           "l2": "no flush (warm)" if flush is None else "flushed before every call"}))
 
 
+def workload_config(spec, args, world):
+    """The workload the line measures (the same dict in both arms)."""
+    return {"workload": spec.name, "batch": spec.batch, "n_q": spec.n_q,
+            "contexts": "50000+800*t, t~U{0..14}" if args.config in (2, 3) else str(spec.first_pos[0]),
+            "n_idx_heads": spec.n_idx_heads, "kv": spec.kv_dtype, "page_size": spec.page_size,
+            "compressed_keys": "in the KV pages" if args.paged_kc else "contiguous per request",
+            "parallelism": f"replicas x{world}"}
+
+
 def prepare_step(qsa, spec, paged_kc=False):
     """Device state of one workload and one checked step, whose selection
     gives the algorithmic byte count. Returns (state, sel_pos on the host,
@@ -719,13 +728,9 @@ def run_ours(args, world, rank):
             "latency_us_p10_p50_p90": [round(float(np.percentile(step_ms, q)) * 1e3, 2) for q in (10, 50, 90)],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "fp8" if spec.kv_dtype == "fp8" else "bf16", "data": "synthetic",
-            "config": {"workload": spec.name, "batch": spec.batch, "n_q": spec.n_q,
-                       "contexts": "50000+800*t, t~U{0..14}" if args.config in (2, 3) else str(spec.first_pos[0]),
-                       "n_idx_heads": spec.n_idx_heads, "kv": spec.kv_dtype, "page_size": spec.page_size,
-                       "compressed_keys": "in the KV pages" if args.paged_kc else "contiguous per request",
-                       "l2": "no flush (warm)" if flush is None else "flushed before every step (a write of 2x L2, then a read of 2x L2)",
-                       "launch": "direct calls" if args.no_graph else "the step captured once as a CUDA graph, replayed",
-                       "parallelism": f"replicas x{world}"},
+            "config": workload_config(spec, args, world),
+            "protocol": {"l2": "no flush (warm)" if flush is None else "flushed before every step (a write of 2x L2, then a read of 2x L2)",
+                         "launch": "direct calls" if args.no_graph else "the step captured once as a CUDA graph, replayed"},
             "bytes_per_step": {"kc": int(b_kc), "kv_union": int(b_kv_union), "kv_sum": int(b_kv_sum)},
             "kernels": kernels, "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
             "cpu_baseline_single_core": cpu1, "sweep": sweep_out,
@@ -782,10 +787,9 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": spec.name, "batch": spec.batch, "n_q": spec.n_q, "kv": spec.kv_dtype,
-                   "n_idx_heads": spec.n_idx_heads, "page_size": spec.page_size,
-                   "step": f"{per_step} whole requests of the batch (cycling over its first {n_saved}), "
-                           f"one per process"},
+        "config": workload_config(spec, args, world),
+        "protocol": {"step": f"{per_step} whole requests of the batch (cycling over its first {n_saved}), "
+                             f"one per process"},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": workers, "kind": "oracle",
                          "sample": f"{n} requests of {spec.name}, {per_step} per step on {workers} processes "
                                    f"(spawn), numpy FP64"},

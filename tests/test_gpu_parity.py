@@ -658,6 +658,39 @@ def test_score_chunk_full_size_sampled(qsa, pad_to):
         assert np.all(np.isnan(sc[0, i, n:])), i
 
 
+@pytest.mark.parametrize("case", ["no_full_block", "tiny_capacity", "one_query", "ragged_by_one", "three_requests"])
+def test_score_chunk_edge_cases(qsa, case):
+    # shapes at the tensor-memory kernel's edges: every tile of a chunk whose
+    # queries see no full block (a CTA's first tile is still copied and
+    # multiplied, and must store nothing), a block capacity below one 128-block
+    # tile, a single query, 129 queries (a second query tile of one), and three
+    # requests of different lengths with three index heads
+    if case == "no_full_block":
+        spec, n_chunk = small_spec([2000], n_q=1, seed=41), 40
+        q_pos = [[i % 3 for i in range(n_chunk)]]  # positions 0..2: no full block yet
+    elif case == "tiny_capacity":
+        spec, n_chunk = small_spec([19], n_q=1, seed=42), 20
+        q_pos = [[i for i in range(n_chunk)]]  # at most 5 full blocks
+    elif case == "one_query":
+        spec, n_chunk = small_spec([3333], n_q=1, n_idx_heads=2, seed=43), 1
+        q_pos = [[3333]]
+    elif case == "ragged_by_one":
+        spec, n_chunk = small_spec([4100], n_q=1, seed=44), 129
+        q_pos = [[4100 - 2 * (n_chunk - 1 - i) for i in range(n_chunk)]]
+    else:
+        spec, n_chunk = small_spec([5000, 700, 2600], n_q=1, n_idx_heads=3, seed=45), 70
+        q_pos = [[max(0, spec.first_pos[r] - 5 * (n_chunk - 1 - i)) for i in range(n_chunk)] for r in range(3)]
+    sc, qi, kcb, ws = _chunk_case(qsa, spec, n_chunk, q_pos, 9300)
+    _check_ok(qsa, ws)
+    for r in range(spec.batch):
+        for i in range(n_chunk):
+            p = q_pos[r][i]
+            n = O.n_full(p)
+            ref = O.score_row(qi[r, i], kcb[r], p)
+            assert np.all(np.abs(sc[r, i, :n] - ref) <= SCORE_RTOL * np.maximum(np.abs(ref), 1.0)), (r, i)
+            assert np.all(np.isnan(sc[r, i, n:])), (r, i)
+
+
 def test_score_chunk_reports_a_bad_position(qsa):
     spec = small_spec([3001], n_q=1, seed=33)
     q_pos = [[-1] + [3001 - 40 + i for i in range(39)]]
