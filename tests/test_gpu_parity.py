@@ -691,6 +691,32 @@ def test_score_chunk_edge_cases(qsa, case):
             assert np.all(np.isnan(sc[r, i, n:])), (r, i)
 
 
+def test_score_chunk_more_tiles_per_cta_than_its_table(qsa):
+    # 16,384 queries against a 100,000-token request: 128 query tiles x 196
+    # block tiles = 25,088 tiles, about 165 per CTA, more than the 128 whose
+    # causal extents a CTA keeps in its table (the rest are computed on the
+    # fly); sampled rows against the oracle, the scores stay on the device
+    B, n_chunk, L = 1, 16384, 100000
+    mb = (L + 3) // 4
+    d = qsa.make_dims(B, 1, mb, 1, 1)
+    ws = qsa.make_workspace(d)
+    kc = synth.normal_bf16((B, mb, 1, 128), 9401, "cuda")
+    qi = synth.normal_bf16((B, n_chunk, 1, 128), 9402, "cuda")
+    pos = [L - 1 - 6 * (n_chunk - 1 - i) for i in range(n_chunk)]
+    qp = torch.tensor([pos], dtype=torch.int32, device="cuda")
+    sc = torch.full((B, n_chunk, mb), float("nan"), device="cuda")
+    qsa.score_chunk(d, qi, kc, qp, sc, ws)
+    _check_ok(qsa, ws)
+    kb, qb = bits(kc), bits(qi)
+    for i in (0, 1, 127, 128, 5000, 8191, 12345, 16255, 16256, 16383):
+        p = pos[i]
+        n = O.n_full(p)
+        ref = O.score_row(qb[0, i], kb[0], p)
+        got = sc[0, i].cpu().numpy()
+        assert np.all(np.abs(got[:n] - ref) <= SCORE_RTOL * np.maximum(np.abs(ref), 1.0)), i
+        assert np.all(np.isnan(got[n:])), i
+
+
 def test_score_chunk_reports_a_bad_position(qsa):
     spec = small_spec([3001], n_q=1, seed=33)
     q_pos = [[-1] + [3001 - 40 + i for i in range(39)]]
