@@ -218,6 +218,21 @@ qsa_status qsa_score_chunk(const qsa_dims* dims, int32_t n_chunk, const void* q_
                                       static_cast<cudaStream_t>(stream)));
 }
 
+qsa_status qsa_test_chunk_timeout(const qsa_dims* dims, int32_t n_chunk, const void* q_idx, const void* kc,
+                                  const int32_t* q_pos, float* scores, void* ws, size_t ws_bytes, void* stream) {
+  qsa_status st = check_dims(dims);
+  if (st != QSA_OK) return st;
+  if (n_chunk < 1 || n_chunk > QSA_MAX_CHUNK) return QSA_ERR_INVALID_ARG;
+  if (!q_idx || !kc || !q_pos || !scores) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(kc) || !aligned_all(4, q_pos, scores)) return QSA_ERR_INVALID_ARG;
+  if ((long long)dims->batch * n_chunk * dims->max_blocks >= (1LL << 40)) return QSA_ERR_UNSUPPORTED;
+  if (dims->batch > 65535) return QSA_ERR_UNSUPPORTED;
+  if ((st = check_ws(dims, ws, ws_bytes, nullptr)) != QSA_OK) return st;
+  return from_cuda(launch_score_chunk(*dims, n_chunk, static_cast<const __nv_bfloat16*>(q_idx),
+                                      static_cast<const __nv_bfloat16*>(kc), q_pos, scores, err_word(ws),
+                                      static_cast<cudaStream_t>(stream), true));
+}
+
 qsa_status qsa_topk(const qsa_dims* dims, const float* scores, const int32_t* q_pos,
                     int32_t* sel_blk, int32_t* sel_pos, void* ws, size_t ws_bytes, void* stream) {
   qsa_status st = check_dims(dims);

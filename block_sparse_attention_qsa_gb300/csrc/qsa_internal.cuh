@@ -169,8 +169,10 @@ cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q
                         int32_t* sel_blk, int32_t* sel_pos, int32_t* err, const int32_t* page_table,
                         int32_t* sel_row, cudaStream_t s, bool pdl);
 // many queries per request (a prefill chunk) against the request's blocks
+// withhold_first_copy: the failure-detection test (qsa_test_chunk_timeout)
 cudaError_t launch_score_chunk(const qsa_dims& d, int n_chunk, const __nv_bfloat16* q_idx, const __nv_bfloat16* kc,
-                               const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s);
+                               const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s,
+                               bool withhold_first_copy = false);
 // draft step: reused selection rows plus the positions since -> cache rows
 cudaError_t launch_draft_resolve(const qsa_dims& d, const int32_t* sel_pos, const int32_t* sel_q_pos, int n_sel,
                                  const int32_t* src, const int32_t* q_pos, const int32_t* page_table,

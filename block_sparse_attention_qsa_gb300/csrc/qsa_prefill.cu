@@ -162,7 +162,8 @@ __global__ void __launch_bounds__(kRoleThreads, 1) score_chunk_kernel(const __gr
                                                                     const __grid_constant__ CUtensorMap tm_q,
                                                                     const int32_t* __restrict__ q_pos,
                                                                     float* __restrict__ scores, int32_t* err,
-                                                                    int n_chunk, int H, int max_blocks, int B) {
+                                                                    int n_chunk, int H, int max_blocks, int B,
+                                                                    int withhold) {
   extern __shared__ uint8_t psm_raw[];
   // stage buffers at a 1,024-byte boundary (the swizzle pattern repeats every 1,024 bytes)
   uint8_t* psm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(psm_raw) + 1023) & ~uintptr_t(1023));
@@ -208,12 +209,15 @@ __global__ void __launch_bounds__(kRoleThreads, 1) score_chunk_kernel(const __gr
     tma_load_3d(base + 2 * kAHalf, &tm_q, h * 128, qt * kTN, r, bar);
     tma_load_3d(base + 2 * kAHalf + kBHalf, &tm_q, h * 128 + 64, qt * kTN, r, bar);
   };
-  // the first tile's first heads go out at once (its ring stages are fresh)
+  // the first tile's first heads go out at once (its ring stages are fresh).
+  // withhold (the failure-detection test only): CTA 0 leaves its first copy
+  // out, so the MMA warp's wait for it runs into the clock limit
   const int pre = min(H, kStages);
+  const bool held = withhold && blockIdx.x == 0;
   if (tid == 0 && (long long)blockIdx.x < n_tiles) {
     int r, qt, bt;
     tile_of(blockIdx.x, r, qt, bt);
-    for (int h = 0; h < pre; ++h) issue(h, h, r, qt, bt);
+    for (int h = held ? 1 : 0; h < pre; ++h) issue(h, h, r, qt, bt);
   }
   for (int k = warp; k < kNfTable; k += kRoleThreads / 32) {
     const long long t = blockIdx.x + (long long)k * gridDim.x;
@@ -261,7 +265,7 @@ __global__ void __launch_bounds__(kRoleThreads, 1) score_chunk_kernel(const __gr
     uint32_t phase = pre == kStages ? 1u : 0u;
     bool issued[kStages] = {};
     uint32_t issued_par[kStages] = {};
-    for (int s = 0; s < pre; ++s) issued[s] = (long long)blockIdx.x < n_tiles;
+    for (int s = 0; s < pre; ++s) issued[s] = (long long)blockIdx.x < n_tiles && !(held && s == 0);
     int k = 0;
     for (long long t = blockIdx.x; t < n_tiles; t += gridDim.x, ++k) {
       int r, qt, bt;
@@ -437,7 +441,8 @@ bool make_map(CUtensorMap* m, const __nv_bfloat16* base, int H, int rows, int B,
 }  // namespace
 
 cudaError_t launch_score_chunk(const qsa_dims& d, int n_chunk, const __nv_bfloat16* q_idx, const __nv_bfloat16* kc,
-                               const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s) {
+                               const int32_t* q_pos, float* scores, int32_t* err, cudaStream_t s,
+                               bool withhold_first_copy) {
   alignas(64) CUtensorMap tm_kc, tm_q;
   if (!make_map(&tm_kc, kc, d.n_idx_heads, d.max_blocks, d.batch, kTM) ||
       !make_map(&tm_q, q_idx, d.n_idx_heads, n_chunk, d.batch, kTN))
@@ -450,7 +455,7 @@ cudaError_t launch_score_chunk(const qsa_dims& d, int n_chunk, const __nv_bfloat
   const long long tiles = (long long)d.batch * ((n_chunk + kTN - 1) / kTN) * ((d.max_blocks + kTM - 1) / kTM);
   const int grid = (int)std::min<long long>(tiles, device_sm_count());
   return launch_k(score_chunk_kernel, dim3(grid), dim3(kRoleThreads), smem, s, false, tm_kc, tm_q, q_pos, scores,
-                  err, n_chunk, d.n_idx_heads, d.max_blocks, d.batch);
+                  err, n_chunk, d.n_idx_heads, d.max_blocks, d.batch, withhold_first_copy ? 1 : 0);
 }
 
 }  // namespace qsa

@@ -33,7 +33,7 @@ EXPORTS = (
     "qsa_workspace_init", "qsa_compress_keys", "qsa_score", "qsa_topk", "qsa_sparse_attn",
     "qsa_decode", "qsa_check_errors", "qsa_sparse_attn_noalloc", "qsa_draft_attn",
     "qsa_compress_keys_paged", "qsa_score_paged", "qsa_decode_paged", "qsa_score_chunk",
-    "qsa_resolve", "qsa_sparse_attn_rows",
+    "qsa_resolve", "qsa_sparse_attn_rows", "qsa_test_chunk_timeout",
 )
 
 MAX_DRAFT_GAP = 64  # QSA_MAX_DRAFT_GAP
@@ -85,6 +85,7 @@ def _load() -> ctypes.CDLL:
         "qsa_score_paged": (I, [D, P, P, P, P, P, P, SZ, P]),
         "qsa_decode_paged": (I, [D, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
         "qsa_score_chunk": (I, [D, ctypes.c_int32, P, P, P, P, P, SZ, P]),
+        "qsa_test_chunk_timeout": (I, [D, ctypes.c_int32, P, P, P, P, P, SZ, P]),
         "qsa_resolve": (I, [D, P, P, P, P, P, SZ, P]),
         "qsa_sparse_attn_rows": (I, [D, P, P, P, P, P, P, P, P, SZ, P]),
     }
@@ -286,6 +287,20 @@ def score_chunk(d: Dims, q_idx, kc, q_pos, scores, ws, stream=None):
     w, n = _ws(d, ws)
     _check(lib.qsa_score_chunk(ctypes.byref(d), n_chunk, _ptr(q_idx), _ptr(kc), _ptr(q_pos), _ptr(scores), w, n,
                                _stream(stream)), "qsa_score_chunk")
+
+
+def test_chunk_timeout(d: Dims, q_idx, kc, q_pos, scores, ws, stream=None):
+    """qsa_test_chunk_timeout: score_chunk with one copy withheld, so that one
+    CTA's bounded wait runs out (about a second); check_errors then reports
+    ERR_TIMEOUT. For failure-detection tests."""
+    n_chunk = int(q_idx.shape[1])
+    _want(q_idx, "q_idx", (d.batch, n_chunk, d.n_idx_heads, d.idx_dim), torch.bfloat16)
+    _want(kc, "kc", (d.batch, d.max_blocks, d.n_idx_heads, d.idx_dim), torch.bfloat16)
+    _want(q_pos, "q_pos", (d.batch, n_chunk), torch.int32)
+    _want(scores, "scores", (d.batch, n_chunk, d.max_blocks), torch.float32)
+    w, n = _ws(d, ws)
+    _check(lib.qsa_test_chunk_timeout(ctypes.byref(d), n_chunk, _ptr(q_idx), _ptr(kc), _ptr(q_pos), _ptr(scores), w,
+                                      n, _stream(stream)), "qsa_test_chunk_timeout")
 
 
 def _want_kc_cache(d: Dims, kc_cache):

@@ -274,6 +274,17 @@ qsa_status qsa_sparse_attn_noalloc(const qsa_dims* dims, const void* q, const vo
 qsa_status qsa_score_chunk(const qsa_dims* dims, int32_t n_chunk, const void* q_idx, const void* kc,
                            const int32_t* q_pos, float* scores, void* ws, size_t ws_bytes, void* stream);
 
+/* Failure-detection test of the bounded waits (no counterpart on the pages):
+ * qsa_score_chunk with the first TMA copy of the kernel's first CTA left out,
+ * so that CTA's wait for it runs into its clock limit (about one second).
+ * The CTA then records the timeout, stops issuing work, waits (bounded) for
+ * its own copies in flight, frees its tensor memory and returns; the other
+ * CTAs finish normally. qsa_check_errors afterwards returns QSA_ERR_TIMEOUT
+ * (kind 5), and the context stays usable. The scores of the first CTA's tiles
+ * are not written. Same arguments and checks as qsa_score_chunk. */
+qsa_status qsa_test_chunk_timeout(const qsa_dims* dims, int32_t n_chunk, const void* q_idx, const void* kc,
+                                  const int32_t* q_pos, float* scores, void* ws, size_t ws_bytes, void* stream);
+
 /* Paged compressed keys (the pages place the selected history "in the
  * cache", 10100.com "第一处"; here the compressed keys live in the KV
  * cache's pages too, found through the same page table). kc_cache is

@@ -717,6 +717,50 @@ def test_score_chunk_more_tiles_per_cta_than_its_table(qsa):
         assert np.all(np.isnan(got[n:])), i
 
 
+def test_chunk_kernel_wait_runs_out_and_reports_a_timeout(qsa):
+    # Failure detection without a fault: the test hook withholds one TMA copy
+    # of the chunked-scoring kernel's first CTA, whose MMA warp then waits for
+    # it until its clock limit (about a second), records a timeout, stops every
+    # role and frees its tensor memory; the other CTAs finish. The timeout is
+    # reported, and the next call on the same context is complete and correct.
+    import time
+
+    spec = small_spec([5003, 2900], n_q=1, seed=51)
+    n_chunk = 150
+    q_pos = [[max(0, spec.first_pos[r] - 3 * (n_chunk - 1 - i)) for i in range(n_chunk)] for r in range(2)]
+    inp = synth.make_inputs(spec)
+    g = _dev(inp)
+    d = qsa.dims_for_spec(spec)
+    ws = qsa.make_workspace(d)
+    kc = torch.zeros((2, spec.max_blocks(), 1, 128), dtype=torch.bfloat16, device="cuda")
+    qsa.compress_keys(d, g["idx_keys"], g["q_pos"], kc, ws)
+    _check_ok(qsa, ws)
+    qi = synth.normal_bf16((2, n_chunk, 1, 128), 9501, device="cuda")
+    qp = torch.tensor(q_pos, dtype=torch.int32, device="cuda")
+    sc = torch.full((2, n_chunk, spec.max_blocks()), float("nan"), device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.time()
+    qsa.test_chunk_timeout(d, qi, kc, qp, sc, ws)
+    torch.cuda.synchronize()
+    waited = time.time() - t0
+    st, info = qsa.check_errors(ws)
+    assert st == qsa.ERR_TIMEOUT and info[0] == 5, info
+    assert 0.2 < waited < 30, waited
+    # the first CTA's tile (request 0, queries 0..127, blocks 0..127) was not written
+    assert torch.isnan(sc[0, :128, :128]).all()
+    sc.fill_(float("nan"))
+    qsa.score_chunk(d, qi, kc, qp, sc, ws)
+    _check_ok(qsa, ws)
+    got, qb, kb = sc.cpu().numpy(), bits(qi), bits(kc)
+    for r in range(2):
+        for i in (0, 1, 77, 127, 128, 149):
+            p = q_pos[r][i]
+            n = O.n_full(p)
+            ref = O.score_row(qb[r, i], kb[r], p)
+            assert np.all(np.abs(got[r, i, :n] - ref) <= SCORE_RTOL * np.maximum(np.abs(ref), 1.0)), (r, i)
+            assert np.all(np.isnan(got[r, i, n:])), (r, i)
+
+
 def test_score_chunk_reports_a_bad_position(qsa):
     spec = small_spec([3001], n_q=1, seed=33)
     q_pos = [[-1] + [3001 - 40 + i for i in range(39)]]
