@@ -3,6 +3,10 @@
 Each .cu under csrc/ compiles to an object in parallel; the objects link into
 ``block_sparse_attention_qsa_gb300/libqsa.so`` with the CUDA runtime linked
 statically, so the library only needs the NVIDIA driver at run time.
+
+``build(trace=True)`` makes the tracing build instead, ``libqsa_trace.so``
+(the same sources with ``-DQSA_TRACE``: the step's kernels record per-CTA
+phase stamps, read back with ``qsa_trace_read``); ``timeline.py`` uses it.
 """
 
 from __future__ import annotations
@@ -19,6 +23,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqsa.so")
+BUILD_TRACE = os.path.join(PKG, "_build_trace")
+LIB_TRACE = os.path.join(PKG, "libqsa_trace.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
@@ -42,17 +48,21 @@ def _newest_input() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link libqsa.so; returns its path. Skips work when the
-    library is newer than every source unless ``force``."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), trace: bool = False) -> str:
+    """Compile and link libqsa.so (or, with ``trace``, libqsa_trace.so);
+    returns its path. Skips work when the library is newer than every source
+    unless ``force``."""
+    lib, bdir = (LIB_TRACE, BUILD_TRACE) if trace else (LIB, BUILD)
+    if trace:
+        extra_flags = (*extra_flags, "-DQSA_TRACE")
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _newest_input():
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
     objs = []
     cmds = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         cmds.append([cc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj])
 
@@ -70,10 +80,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         for lg in logs:
             if lg.strip():
                 print(lg)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     run([cc, *ARCH, "-shared", "-o", tmp, *objs])
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -5,6 +5,7 @@
 #include <algorithm>
 
 #include "qsa_internal.cuh"
+#include "qsa_trace.cuh"
 
 namespace qsa {
 
@@ -231,6 +232,21 @@ qsa_status qsa_test_chunk_timeout(const qsa_dims* dims, int32_t n_chunk, const v
   return from_cuda(launch_score_chunk(*dims, n_chunk, static_cast<const __nv_bfloat16*>(q_idx),
                                       static_cast<const __nv_bfloat16*>(kc), q_pos, scores, err_word(ws),
                                       static_cast<cudaStream_t>(stream), true));
+}
+
+qsa_status qsa_trace_read(int32_t kernel, uint64_t* host, int32_t n_ctas, int32_t clear) {
+  if (n_ctas < 0 || n_ctas > kTraceCtas || (n_ctas > 0 && !host)) return QSA_ERR_INVALID_ARG;
+  static_assert(QSA_TRACE_SLOTS == kTraceSlots, "trace record size");
+  unsigned long long* h = reinterpret_cast<unsigned long long*>(host);
+  cudaError_t e;
+  switch (kernel) {
+    case QSA_TRACE_SCORE: e = trace_score(h, n_ctas, clear != 0); break;
+    case QSA_TRACE_TOPK: e = trace_topk(h, n_ctas, clear != 0); break;
+    case QSA_TRACE_ATTN: e = trace_attn(h, n_ctas, clear != 0); break;
+    default: return QSA_ERR_INVALID_ARG;
+  }
+  if (e == cudaErrorNotSupported) return QSA_ERR_UNSUPPORTED;
+  return from_cuda(e);
 }
 
 qsa_status qsa_topk(const qsa_dims* dims, const float* scores, const int32_t* q_pos,

@@ -43,9 +43,12 @@
 // arrive, counted by an atomic ticket, merges them and resets the ticket, so
 // there is no spin-wait anywhere.
 #include "qsa_internal.cuh"
+#include "qsa_trace.cuh"
 
 namespace qsa {
 namespace {
+
+QSA_TRACE_TABLE
 
 constexpr int kTile = 64;       // BF16 positions per CTA step: 4 warps of 16 (FP8: 4 of 32)
 // resident CTAs per SM: BF16 rows take twice the registers of FP8 codes
@@ -246,8 +249,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
   const uint8_t* vbase = static_cast<const uint8_t*>(a.v_cache);
 
   const int cta = blockIdx.x;
+  QSA_MARK(0);
   const long long w0 = tile_begin(a, cta), w1 = tile_begin(a, cta + 1);
   if (w0 >= w1) {
+    QSA_MARK(3);
     pdl_trigger();
     return;
   }
@@ -264,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
   asm volatile("cp.async.commit_group;" ::: "memory");
 
   pdl_wait();  // the selection is
+  QSA_MARK(1);
 
   // Row look-ahead: the selection entries of tile w + 2 are loaded while tile w
   // is processed, and turn into cache rows for the K/V loads of tile w + 1.
@@ -484,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
     }
 
     // ---- merge the 4 warps (the next unit's first K/V rows are in flight) ----
+    QSA_MARK_LAST(2);
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       l_run[0] += __shfl_xor_sync(kFull, l_run[0], o);
@@ -566,6 +573,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
         __threadfence();
         s_last = (atomicAdd(&a.tickets[u], 1) == n_piece - 1);
       }
+      QSA_MARK(5);
       __syncthreads();
       if (s_last) {
         __threadfence();
@@ -623,12 +631,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
           orow[h * kDim + tid] = __float2bfloat16_rn(l > 0.f ? o[h] / l * vscale : 0.f);
         }
         if (tid == 0) a.tickets[u] = 0;  // ready for the next launch
+        QSA_MARK(6);
       }
     }
     if (!more) break;
     ++u;
     t = 0;
   }
+  QSA_MARK(3);
   pdl_trigger();
 }
 
@@ -716,6 +726,8 @@ int page_shift_of(int page_size) {
 }
 
 }  // namespace
+
+QSA_TRACE_HOST(trace_attn)
 
 AttnPlan attn_plan(const qsa_dims& d, int num_sms) {
   AttnPlan pl;

@@ -13,9 +13,12 @@
 // from the loaded registers, so the key tile is shared by the 4 queries in
 // registers rather than in shared memory and the ALUs stay idle.
 #include "qsa_internal.cuh"
+#include "qsa_trace.cuh"
 
 namespace qsa {
 namespace {
+
+QSA_TRACE_TABLE
 
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -150,7 +153,9 @@ __global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(cons
   extern __shared__ int s_off[];  // [B + 1] first unit (16 blocks) of each request
   int* s_nb = s_off + B + 1;      // [B] full blocks of each request (its longest query)
 
+  QSA_MARK(0);
   pdl_wait();  // no-op unless launched as a dependent
+  QSA_MARK(1);
   // Let the selector launch now: its CTAs take each SM as this kernel's CTA
   // there exits, and its own wait still covers all of this grid's scores.
   pdl_trigger();
@@ -306,6 +311,8 @@ __global__ void __launch_bounds__(256, ScoreGeom<H>::MIN_CTAS) score_kernel(cons
     }
     u = seg_end;  // the unrolled loop may step past the end of this request's units
   }
+  QSA_MARK_LAST(2);
+  QSA_MARK_LAST(3);
 }
 
 int shift_of(int x) {
@@ -349,6 +356,8 @@ cudaError_t launch_score_h(const qsa_dims& d, const __nv_bfloat16* q_idx, const 
 }
 
 }  // namespace
+
+QSA_TRACE_HOST(trace_score)
 
 cudaError_t launch_compress(const qsa_dims& d, const __nv_bfloat16* idx_keys, const int32_t* q_pos,
                             const int32_t* block_lo, __nv_bfloat16* kc, int32_t* err,

@@ -29,9 +29,12 @@
 // for a CTA's first row) so the cache rows written inside qsa_decode need no
 // dependent global loads.
 #include "qsa_internal.cuh"
+#include "qsa_trace.cuh"
 
 namespace qsa {
 namespace {
+
+QSA_TRACE_TABLE
 
 constexpr int kThreads = 1024;
 constexpr unsigned kFull = 0xffffffffu;
@@ -285,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
   uint32_t* body = sm + kHdrWords;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
+  QSA_MARK(0);
 
   // Inputs of a row that do not come from the score kernel: its position and
   // its request's page table (staged when it fits).
@@ -306,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
   if (blockIdx.x < rows) stage_row(blockIdx.x);
 
   pdl_wait();  // the scores come from the previous kernel
+  QSA_MARK(1);
   // Let the attention kernel launch now: its CTAs wait on the SMs this grid
   // leaves free, and their own wait still covers every selection written here.
   pdl_trigger();
@@ -453,6 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
       }
     }
     __syncthreads();  // the selection list is complete
+    QSA_MARK(2);
     // outputs, coalesced: block ids, their positions (then the unfilled block's), cache rows
     if (ob)
       for (int i = tid; i < kTopK; i += kThreads) ob[i] = blk[i];
@@ -467,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
     for (int i = tid; i < 2 * kHistBins; i += kThreads) hist[i] = 0;
     __syncthreads();  // shared memory is reused by the next row
   }
+  QSA_MARK(3);
 }
 
 
@@ -524,6 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const float* 
   const uint32_t crank = cluster_rank(), C = cluster_size();
   const int row = blockIdx.x / (int)C;
   const int r = row / n_q, j = row - r * n_q;
+  QSA_MARK(0);
 
   // inputs that do not come from the score kernel
   const int p = q_pos[row];
@@ -537,6 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const float* 
   }
   for (int i = tid; i < 4096; i += kThreads) hist[i] = 0;  // hist and hist2
   pdl_wait();  // the scores come from the previous kernel
+  QSA_MARK(1);
   pdl_trigger();
   __syncthreads();
 
@@ -556,6 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const float* 
       if (orow)
         for (int i = tid; i < kWidth; i += kThreads) orow[i] = (p_ok && i <= p) ? row_of(ro, pt, r, i, err, j) : -1;
     }
+    QSA_MARK(3);
     cluster_sync();
     return;
   }
@@ -642,6 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const float* 
       tie_m |= (uint32_t)(in && !whole && key[e] == T) << e;
     }
   }
+  QSA_MARK(2);
   // this CTA's counts in index order, then the CTAs before it in the cluster.
   // Inside one CTA the packed (ties << 16 | selected) scan cannot overflow: a
   // CTA holds at most 32 x 1024 keys and selects at most kTopK. Summed over
@@ -687,6 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_cluster_kernel(const float* 
     if (op) op[kBlock * kTopK + tid] = pos;
     if (orow) orow[kBlock * kTopK + tid] = pos < 0 ? -1 : row_of(ro, pt, r, pos, err, j);
   }
+  QSA_MARK(3);
   cluster_sync();  // no CTA leaves while another may still read its counts
 }
 
@@ -714,6 +726,8 @@ cudaError_t launch_topk_cluster(int C, int rows, const float* scores, const int3
 }
 
 }  // namespace
+
+QSA_TRACE_HOST(trace_topk)
 
 cudaError_t launch_topk(const qsa_dims& d, const float* scores, const int32_t* q_pos,
                         int32_t* sel_blk, int32_t* sel_pos, int32_t* err, const int32_t* page_table,

@@ -6,7 +6,9 @@ memory; the stream is torch's current stream unless one is given. Shapes and
 dtypes are checked here because the C ABI receives bare pointers.
 
 Importing this module loads the library and raises ImportError if it is
-missing or was built for another ABI: there is no CPU fallback.
+missing or was built for another ABI: there is no CPU fallback. The
+environment variable QSA_LIBRARY names another build to load instead (the
+tracing build, libqsa_trace.so, for timeline.py).
 """
 
 from __future__ import annotations
@@ -16,10 +18,11 @@ import math
 import os
 from typing import Optional, Tuple
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libqsa.so")
+LIB_PATH = os.environ.get("QSA_LIBRARY") or os.path.join(_HERE, "libqsa.so")
 ABI_VERSION = 1
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_BAD_INDEX, ERR_TIMEOUT, ERR_CUDA = range(7)
@@ -33,8 +36,10 @@ EXPORTS = (
     "qsa_workspace_init", "qsa_compress_keys", "qsa_score", "qsa_topk", "qsa_sparse_attn",
     "qsa_decode", "qsa_check_errors", "qsa_sparse_attn_noalloc", "qsa_draft_attn",
     "qsa_compress_keys_paged", "qsa_score_paged", "qsa_decode_paged", "qsa_score_chunk",
-    "qsa_resolve", "qsa_sparse_attn_rows", "qsa_test_chunk_timeout",
+    "qsa_resolve", "qsa_sparse_attn_rows", "qsa_test_chunk_timeout", "qsa_trace_read",
 )
+TRACE_SCORE, TRACE_TOPK, TRACE_ATTN = 0, 1, 2  # qsa_trace_read tables
+TRACE_SLOTS, TRACE_CTAS = 8, 4096
 
 MAX_DRAFT_GAP = 64  # QSA_MAX_DRAFT_GAP
 MAX_CHUNK = 65536  # QSA_MAX_CHUNK
@@ -88,6 +93,7 @@ def _load() -> ctypes.CDLL:
         "qsa_test_chunk_timeout": (I, [D, ctypes.c_int32, P, P, P, P, P, SZ, P]),
         "qsa_resolve": (I, [D, P, P, P, P, P, SZ, P]),
         "qsa_sparse_attn_rows": (I, [D, P, P, P, P, P, P, P, P, SZ, P]),
+        "qsa_trace_read": (I, [ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -301,6 +307,16 @@ def test_chunk_timeout(d: Dims, q_idx, kc, q_pos, scores, ws, stream=None):
     w, n = _ws(d, ws)
     _check(lib.qsa_test_chunk_timeout(ctypes.byref(d), n_chunk, _ptr(q_idx), _ptr(kc), _ptr(q_pos), _ptr(scores), w,
                                       n, _stream(stream)), "qsa_test_chunk_timeout")
+
+
+def trace_read(kernel: int, n_ctas: int = TRACE_CTAS, clear: bool = False):
+    """qsa_trace_read: the per-CTA phase stamps of a kernel's latest launch
+    as a numpy uint64 array [n_ctas][TRACE_SLOTS] (tracing build only; the
+    product build raises QSAError with ERR_UNSUPPORTED). clear zeroes the
+    table afterwards; n_ctas 0 only clears."""
+    buf = np.zeros((n_ctas, TRACE_SLOTS), dtype=np.uint64)
+    _check(lib.qsa_trace_read(kernel, buf.ctypes.data if n_ctas else None, n_ctas, int(clear)), "qsa_trace_read")
+    return buf
 
 
 def _want_kc_cache(d: Dims, kc_cache):

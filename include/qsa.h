@@ -285,6 +285,24 @@ qsa_status qsa_score_chunk(const qsa_dims* dims, int32_t n_chunk, const void* q_
 qsa_status qsa_test_chunk_timeout(const qsa_dims* dims, int32_t n_chunk, const void* q_idx, const void* kc,
                                   const int32_t* q_pos, float* scores, void* ws, size_t ws_bytes, void* stream);
 
+/* Phase timeline of the fused step's kernels (tracing; no counterpart on the
+ * pages). Only the tracing build of the library (libqsa_trace.so, compiled
+ * with -DQSA_TRACE) records anything; the product build returns
+ * QSA_ERR_UNSUPPORTED and has no marks in its kernels. kernel selects the
+ * table: QSA_TRACE_SCORE (qsa_score's kernel), QSA_TRACE_TOPK (the
+ * selector, either form) or QSA_TRACE_ATTN (the attention kernel). Each CTA
+ * below 4,096 of the kernel's most recent launches owns QSA_TRACE_SLOTS
+ * uint64 words: %globaltimer (ns) at its start [0], at the release of its
+ * wait on the previous kernel [1], when its main work was done [2] (the
+ * latest of its warps where they finish apart), at its end [3], its SM id
+ * plus one [4], and for attention the time it published a piece of a split
+ * unit [5] and finished a merge of pieces [6]; a slot not reached is 0 (the
+ * caller zeroes the tables with clear). host: n_ctas * QSA_TRACE_SLOTS words,
+ * or null (with n_ctas 0) to only clear. Synchronous: waits for the device.
+ * 0 <= n_ctas <= 4,096, else QSA_ERR_INVALID_ARG. */
+enum { QSA_TRACE_SCORE = 0, QSA_TRACE_TOPK = 1, QSA_TRACE_ATTN = 2, QSA_TRACE_SLOTS = 8 };
+qsa_status qsa_trace_read(int32_t kernel, uint64_t* host, int32_t n_ctas, int32_t clear);
+
 /* Paged compressed keys (the pages place the selected history "in the
  * cache", 10100.com "第一处"; here the compressed keys live in the KV
  * cache's pages too, found through the same page table). kc_cache is
