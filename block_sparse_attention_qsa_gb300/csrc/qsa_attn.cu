@@ -78,6 +78,13 @@ __device__ __forceinline__ uint4 ldg16(const void* p) {
   return v;
 }
 
+// atomic add of 1 with acquire-release semantics at GPU scope; returns the old value
+__device__ __forceinline__ int ticket_acq_rel(int32_t* p) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+  return old;
+}
+
 // a 32-bit load issued at this point of the program (its use may come much later)
 __device__ __forceinline__ int ld_issue(const int32_t* p) {
   int v;
@@ -566,17 +573,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
       for (int h = 0; h < 8; ++h) part[16 + h * kDim + tid] = o[h];
       const long long uw0 = (long long)u * a.tiles;
       const int c_first = cta_of_tile(a, uw0), n_piece = cta_of_tile(a, uw0 + a.tiles - 1) - c_first + 1;
-      // the barrier orders every thread's stores of the piece before thread 0's
-      // fence, which makes them visible before the ticket is taken
+      // The barrier orders every thread's stores of the piece before thread 0's
+      // ticket, an acquire-release add at GPU scope: its release makes them
+      // (cumulatively) visible to whoever takes a later ticket, and for the
+      // CTA that takes the last one its acquire, passed on by the barrier
+      // after it, orders every thread's reads of the other pieces after all
+      // of their releases.
       __syncthreads();
-      if (tid == 0) {
-        __threadfence();
-        s_last = (atomicAdd(&a.tickets[u], 1) == n_piece - 1);
-      }
+      if (tid == 0) s_last = (ticket_acq_rel(&a.tickets[u]) == n_piece - 1);
       QSA_MARK(5);
       __syncthreads();
       if (s_last) {
-        __threadfence();
         // every piece's (max, sum) at once, with the first kMergeBatch pieces'
         // accumulators already on their way; then the rest kMergeBatch at a time
         float* pm = wacc;                        // [n_piece][8] (the merge buffer is free now)
