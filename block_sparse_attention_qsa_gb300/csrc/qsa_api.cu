@@ -26,6 +26,7 @@ WsLayout ws_layout(const qsa_dims& d, int num_sms) {
   w.units = pl.units;
   w.tiles = pl.tiles;
   w.grid = pl.grid;
+  w.cl = pl.cl;
   qsa_dims dd = d;  // a draft step's wider selection may take more CTAs
   dd.width = kDraftWidth;
   const int grid_max = std::max(pl.grid, attn_plan(dd, num_sms).grid);
@@ -275,7 +276,7 @@ qsa_status qsa_sparse_attn(const qsa_dims* dims, const void* q, const void* k_ca
     return QSA_ERR_INVALID_ARG;
   WsLayout w;
   if ((st = check_ws(dims, ws, ws_bytes, &w)) != QSA_OK) return st;
-  const AttnPlan pl{w.units, w.tiles, w.grid};
+  const AttnPlan pl{w.units, w.tiles, w.grid, w.cl};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* srow = at<int32_t>(ws, w.sel_row);
   if (launch_resolve(*dims, sel_pos, q_pos, page_table, srow, err_word(ws), s) != cudaSuccess)
@@ -307,7 +308,7 @@ qsa_status qsa_sparse_attn_rows(const qsa_dims* dims, const void* q, const void*
   if (!aligned_all(4, k_scale, v_scale, sel_row) || !aligned_all(2, out)) return QSA_ERR_INVALID_ARG;
   WsLayout w;
   if ((st = check_ws(dims, ws, ws_bytes, &w)) != QSA_OK) return st;
-  const AttnPlan pl{w.units, w.tiles, w.grid};
+  const AttnPlan pl{w.units, w.tiles, w.grid, w.cl};
   return from_cuda(launch_attn(*dims, q, k_cache, v_cache, k_scale, v_scale, sel_row, out,
                                at<int32_t>(ws, w.tickets), at<float>(ws, w.partials), pl,
                                static_cast<cudaStream_t>(stream), true));
@@ -345,7 +346,7 @@ qsa_status decode_impl(const qsa_dims* dims, const void* q_idx, const void* kc, 
   // block ids and positions only when the caller asked for them; attention needs the cache rows
   e = launch_topk(*dims, sc, q_pos, sel_blk, sel_pos, err_word(ws), page_table, srow, s, true);
   if (e != cudaSuccess) return QSA_ERR_CUDA;
-  const AttnPlan pl{w.units, w.tiles, w.grid};
+  const AttnPlan pl{w.units, w.tiles, w.grid, w.cl};
   e = launch_attn(*dims, q, k_cache, v_cache, k_scale, v_scale, srow, out, at<int32_t>(ws, w.tickets),
                   at<float>(ws, w.partials), pl, s, true);
   return from_cuda(e);

@@ -42,6 +42,8 @@
 // publishes (max, sum, acc) pieces to the workspace and the last piece to
 // arrive, counted by an atomic ticket, merges them and resets the ticket, so
 // there is no spin-wait anywhere.
+#include <algorithm>
+
 #include "qsa_internal.cuh"
 #include "qsa_trace.cuh"
 
@@ -65,6 +67,7 @@ constexpr int kRowsPerLane = FP8 ? 4 : 2;
 template <bool FP8>
 constexpr int kMinTilesPerCta = FP8 ? 2 : 3;
 constexpr int kMergeBatch = 4;  // pieces whose accumulators are read at once
+constexpr int kMaxCluster = 16;  // CTAs per unit in the cluster form (non-portable above 8)
 constexpr int kThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -216,6 +219,7 @@ struct AttnArgs {
   float* partials;
   long long total;  // units * tiles: the tile stream the CTAs share
   int tiles, grid, n_kv, page_size, width;
+  int cl;  // cluster form: CTAs per unit (its cluster), else 0
   float sm_scale;
 };
 
@@ -232,7 +236,12 @@ struct Cursor {
   int t, g, row;
 };
 
-template <bool FP8>
+// CL: the cluster form for few units. Each unit is one thread-block cluster
+// of a.cl CTAs, CTA k taking the unit's tiles [k T / cl, (k+1) T / cl); the
+// CTAs' pieces stay in their shared memory and are merged through
+// distributed shared memory between two cluster barriers (each CTA merges
+// 1 / cl of the unit's outputs), with no workspace, fence or ticket.
+template <bool FP8, bool CL>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const AttnArgs a) {
   __shared__ __align__(16) __nv_bfloat16 sQ[2][kGroup * kDim];
   __shared__ __align__(16) float wacc[4 * kGroup * kDim];  // [warp][head][dim]
@@ -257,8 +266,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
 
   const int cta = blockIdx.x;
   QSA_MARK(0);
-  const long long w0 = tile_begin(a, cta), w1 = tile_begin(a, cta + 1);
-  if (w0 >= w1) {
+  long long w0, w1;
+  if constexpr (CL) {
+    // one unit per cluster (the host keeps cl <= tiles, so no share is empty)
+    const int uu = cta / a.cl, rk = cta - uu * a.cl;
+    w0 = (long long)uu * a.tiles + (long long)rk * a.tiles / a.cl;
+    w1 = (long long)uu * a.tiles + (long long)(rk + 1) * a.tiles / a.cl;
+  } else {
+    w0 = tile_begin(a, cta);
+    w1 = tile_begin(a, cta + 1);
+  }
+  if (!CL && w0 >= w1) {
     QSA_MARK(3);
     pdl_trigger();
     return;
@@ -326,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
     const int row = u / a.n_kv, g = u - row * a.n_kv;
     const long long seg_w0 = w;
     const int seg = (int)min((long long)(a.tiles - t), w1 - w);
-    const bool more = w + seg < w1;  // the share continues with unit u + 1
+    const bool more = !CL && w + seg < w1;  // the share continues with unit u + 1 (never in the cluster form)
     if (more) stage_q(u + 1, buf ^ 1);
     asm volatile("cp.async.commit_group;" ::: "memory");
     asm volatile("cp.async.wait_group 1;" ::: "memory");  // this unit's query has landed
@@ -553,13 +571,53 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
              wacc[(2 * 8 + h) * kDim + tid] + wacc[(3 * 8 + h) * kDim + tid];
     __nv_bfloat16* orow = a.out + ((size_t)row * n_q_heads + g * kGroup) * kDim;
 
-    if (t == 0 && seg == a.tiles) {
+    if (!CL && t == 0 && seg == a.tiles) {
       // the whole unit is in this share: write the output
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
         const float l = sL[h];
         orow[h * kDim + tid] = __float2bfloat16_rn(l > 0.f ? o[h] / l * vscale : 0.f);
       }
+    } else if constexpr (CL) {
+      // ---- the cluster's pieces: this CTA's (sM, sL) and accumulators stay in
+      // its shared memory; after the barrier each CTA merges its share of the
+      // unit's 8 x 128 outputs from every CTA's piece ----
+      float* pacc = wacc;  // [8][128] (free once every thread has summed its o[])
+      __syncthreads();
+#pragma unroll
+      for (int h = 0; h < 8; ++h) pacc[h * kDim + tid] = o[h];
+      cluster_sync();
+      const int C = a.cl, rk = (int)cluster_rank();
+      const int per = (kGroup * kDim + C - 1) / C, o_end = min(kGroup * kDim, (rk + 1) * per);
+      for (int oi = rk * per + tid; oi < o_end; oi += kThreads) {
+        const int h = oi / kDim, dd = oi - h * kDim;
+        float mj[kMaxCluster], lj[kMaxCluster], aj[kMaxCluster];
+#pragma unroll
+        for (int j = 0; j < kMaxCluster; ++j) {
+          if (j < C) {
+            mj[j] = ld_peer_f32(peer_addr(sM + h, j));
+            lj[j] = ld_peer_f32(peer_addr(sL + h, j));
+            aj[j] = ld_peer_f32(peer_addr(pacc + oi, j));
+          }
+        }
+        float M = kNegInf;
+#pragma unroll
+        for (int j = 0; j < kMaxCluster; ++j)
+          if (j < C) M = fmaxf(M, mj[j]);
+        const float Mb = M == kNegInf ? 0.f : M;
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxCluster; ++j) {
+          if (j < C) {
+            const float f = exp2f(mj[j] - Mb);
+            L += lj[j] * f;
+            O += aj[j] * f;
+          }
+        }
+        orow[h * kDim + dd] = __float2bfloat16_rn(L > 0.f ? O / L * vscale : 0.f);
+      }
+      QSA_MARK(6);
+      cluster_sync();  // no CTA leaves while another may still read its piece
     } else {
       // ---- a piece of the unit: publish it, the last piece to arrive merges ----
       // slot 2c: the share's first segment, 2c + 1: its last (only these two can be pieces)
@@ -736,6 +794,10 @@ int page_shift_of(int page_size) {
 
 QSA_TRACE_HOST(trace_attn)
 
+// whether clusters of n attention CTAs can be placed on the current device,
+// per cache type (1 yes, 2 no)
+DeviceSlots cluster_ok[2][kMaxCluster + 1];
+
 AttnPlan attn_plan(const qsa_dims& d, int num_sms) {
   AttnPlan pl;
   pl.units = d.batch * d.n_q * d.n_kv_heads;
@@ -747,6 +809,21 @@ AttnPlan attn_plan(const qsa_dims& d, int num_sms) {
   const int min_tiles = d.kv_dtype == QSA_KV_FP8_E4M3 ? kMinTilesPerCta<true> : kMinTilesPerCta<false>;
   const long long most = (total + min_tiles - 1) / min_tiles;
   pl.grid = (int)(most < resident ? most : resident);
+  // The cluster form where it gives no CTA more tiles than stream-K's largest
+  // share and its clusters take at most 4/5 of the resident CTA slots: few
+  // units (small batches), each split over up to kMaxCluster CTAs. Its CTAs'
+  // pieces merge through distributed shared memory instead of the workspace
+  // (pl.grid keeps the stream-K count, which the workspace is sized for and
+  // which the launch falls back to). Measured at batch 8 (64 units, clusters
+  // of 7 filling 448 of 456 slots) the cluster form was slower, 41.7 -> 49.7
+  // us per step: clusters must fit inside one GPC, so a nearly full grid
+  // does not place in one wave.
+  pl.cl = 0;
+  const long long share = (total + pl.grid - 1) / pl.grid;
+  long long c = std::min<long long>(kMaxCluster, (pl.tiles + min_tiles - 1) / min_tiles);
+  c = std::min<long long>(c, resident * 4 / 5 / std::max(pl.units, 1));
+  c = std::min<long long>(c, pl.tiles);
+  if (c >= 2 && (pl.tiles + c - 1) / c <= share) pl.cl = (int)c;
   return pl;
 }
 
@@ -787,9 +864,47 @@ cudaError_t launch_attn(const qsa_dims& d, const void* q, const void* k_cache, c
   a.page_size = d.page_size;
   a.width = d.width;
   a.sm_scale = d.sm_scale > 0.f ? d.sm_scale : 1.0f / sqrtf((float)d.head_dim);
-  if (d.kv_dtype == QSA_KV_FP8_E4M3)
-    return launch_k(attn_kernel<true>, dim3(plan.grid), dim3(kThreads), 0, s, pdl, a);
-  return launch_k(attn_kernel<false>, dim3(plan.grid), dim3(kThreads), 0, s, pdl, a);
+  a.cl = 0;
+  const bool fp8 = d.kv_dtype == QSA_KV_FP8_E4M3;
+  if (plan.cl > 1 && plan.cl <= kMaxCluster && plan.cl <= plan.tiles) {
+    // one cluster of cl CTAs per unit, if the device can place such clusters
+    // (checked once per device and size; else the stream-K form below)
+    auto kern = fp8 ? attn_kernel<true, true> : attn_kernel<false, true>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.units * plan.cl);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = plan.cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    const int placeable = cluster_ok[fp8 ? 1 : 0][plan.cl].get([&] {
+      if (plan.cl > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 2;
+      }
+      cudaLaunchConfig_t one = cfg;
+      one.numAttrs = 1;  // the cluster shape alone
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &one) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 2;
+      }
+      return n > 0 ? 1 : 2;  // 1: placeable, 2: not (both cached)
+    });
+    if (placeable == 1) {
+      a.cl = plan.cl;
+      return cudaLaunchKernelEx(&cfg, kern, a);
+    }
+  }
+  if (fp8) return launch_k(attn_kernel<true, false>, dim3(plan.grid), dim3(kThreads), 0, s, pdl, a);
+  return launch_k(attn_kernel<false, false>, dim3(plan.grid), dim3(kThreads), 0, s, pdl, a);
 }
 
 }  // namespace qsa

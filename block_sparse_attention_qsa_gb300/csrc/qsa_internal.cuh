@@ -43,18 +43,20 @@ constexpr int kPartFloats = 2 * kGroup + kGroup * kDim;  // m[8], l[8], acc[8][1
 
 struct WsLayout {
   size_t tickets, partials, scores, sel_row, total;
-  int units, tiles, grid;
+  int units, tiles, grid, cl;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Work plan of the attention kernel (shared by sizing and launch): the
-// units * tiles 32-position tiles form one stream, cut into `grid` contiguous
-// shares of equal length, one per CTA.
+// units * tiles tiles form one stream, cut into `grid` contiguous shares of
+// equal length, one per CTA (stream-K); or, for few units, each unit is one
+// cluster of `cl` CTAs.
 struct AttnPlan {
-  int units;  // batch * n_q * n_kv_heads
-  int tiles;  // 32-position tiles per unit
-  int grid;   // CTAs
+  int units;   // batch * n_q * n_kv_heads
+  int tiles;   // tiles of selected positions per unit
+  int grid;    // CTAs of the stream-K form
+  int cl = 0;  // > 1: the cluster form, cl CTAs (one cluster) per unit
 };
 AttnPlan attn_plan(const qsa_dims& d, int num_sms);
 WsLayout ws_layout(const qsa_dims& d, int num_sms);
@@ -114,6 +116,34 @@ __device__ __forceinline__ void record_error(int32_t* hdr, int32_t kind, int32_t
 }
 
 __device__ __forceinline__ int n_full_of(int p) { return (p + 1) >> 2; }
+
+// thread-block clusters: rank, size, the hardware barrier (release / acquire),
+// and loads from another CTA's shared memory (distributed shared memory)
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// address of `p` (this CTA's shared memory) in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+  return a;
+}
+__device__ __forceinline__ uint32_t ld_peer(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float ld_peer_f32(uint32_t addr) { return __uint_as_float(ld_peer(addr)); }
 
 // Order-preserving 32-bit key of a score: a larger score has a larger key;
 // -0.0 maps like +0.0 and NaN below every number. The top 11 bits are the

@@ -486,30 +486,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restri
 // CTA the global slots of its picks, which it writes directly. The hardware
 // cluster barrier is the only wait.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// address of `p` (this CTA's shared memory) in CTA `rank` of the cluster
-__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
-  uint32_t a;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
-  return a;
-}
-__device__ __forceinline__ uint32_t ld_peer(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
 
 constexpr int kClHdrWords = 2048 + 2048 + 2048 + 64 + 8 + 8 + kPtCap;  // hist, hist2, sum, wsum, res, cnt, pt
 
