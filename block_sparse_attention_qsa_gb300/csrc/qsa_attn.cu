@@ -588,33 +588,49 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
       for (int h = 0; h < 8; ++h) pacc[h * kDim + tid] = o[h];
       cluster_sync();
       const int C = a.cl, rk = (int)cluster_rank();
-      const int per = (kGroup * kDim + C - 1) / C, o_end = min(kGroup * kDim, (rk + 1) * per);
-      for (int oi = rk * per + tid; oi < o_end; oi += kThreads) {
-        const int h = oi / kDim, dd = oi - h * kDim;
-        float mj[kMaxCluster], lj[kMaxCluster], aj[kMaxCluster];
-#pragma unroll
-        for (int j = 0; j < kMaxCluster; ++j) {
-          if (j < C) {
-            mj[j] = ld_peer_f32(peer_addr(sM + h, j));
-            lj[j] = ld_peer_f32(peer_addr(sL + h, j));
-            aj[j] = ld_peer_f32(peer_addr(pacc + oi, j));
-          }
-        }
+      // every piece's (max, sum) once, into this CTA's [C][16] table (beside
+      // pacc: no peer reads it)
+      float* pml = wacc + kGroup * kDim;
+      for (int i = tid; i < 16 * C; i += kThreads) {
+        const int j = i >> 4, e = i & 15;
+        pml[i] = ld_peer_f32(peer_addr(e < 8 ? sM + e : sL + (e - 8), j));
+      }
+      __syncthreads();
+      // this CTA's outputs, four consecutive dims of one head per thread
+      constexpr int kQuads = kGroup * kDim / 4;
+      const int per = (kQuads + C - 1) / C, q_end = min(kQuads, (rk + 1) * per);
+      for (int qd = rk * per + tid; qd < q_end; qd += kThreads) {
+        const int oi = 4 * qd, h = oi / kDim;
         float M = kNegInf;
-#pragma unroll
-        for (int j = 0; j < kMaxCluster; ++j)
-          if (j < C) M = fmaxf(M, mj[j]);
+        for (int j = 0; j < C; ++j) M = fmaxf(M, pml[16 * j + h]);
         const float Mb = M == kNegInf ? 0.f : M;
-        float L = 0.f, O = 0.f;
+        float L = 0.f, O0 = 0.f, O1 = 0.f, O2 = 0.f, O3 = 0.f;
 #pragma unroll
         for (int j = 0; j < kMaxCluster; ++j) {
           if (j < C) {
-            const float f = exp2f(mj[j] - Mb);
-            L += lj[j] * f;
-            O += aj[j] * f;
+            const float4 x = ld_peer_v4(peer_addr(pacc + oi, j));
+            const float f = exp2f(pml[16 * j + h] - Mb);
+            L += pml[16 * j + 8 + h] * f;
+            O0 += x.x * f;
+            O1 += x.y * f;
+            O2 += x.z * f;
+            O3 += x.w * f;
           }
         }
-        orow[h * kDim + dd] = __float2bfloat16_rn(L > 0.f ? O / L * vscale : 0.f);
+        const float sc = L > 0.f ? vscale / L : 0.f;
+        __nv_bfloat16* dst = orow + oi;  // dims oi .. oi + 3 of head h
+        if ((reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(O0 * sc, O1 * sc), hi = __floats2bfloat162_rn(O2 * sc, O3 * sc);
+          uint2 pk;
+          memcpy(&pk.x, &lo, 4);
+          memcpy(&pk.y, &hi, 4);
+          *reinterpret_cast<uint2*>(dst) = pk;
+        } else {  // an output buffer aligned to 2 bytes only
+          dst[0] = __float2bfloat16_rn(O0 * sc);
+          dst[1] = __float2bfloat16_rn(O1 * sc);
+          dst[2] = __float2bfloat16_rn(O2 * sc);
+          dst[3] = __float2bfloat16_rn(O3 * sc);
+        }
       }
       QSA_MARK(6);
       cluster_sync();  // no CTA leaves while another may still read its piece

@@ -144,6 +144,11 @@ __device__ __forceinline__ uint32_t ld_peer(uint32_t addr) {
   return v;
 }
 __device__ __forceinline__ float ld_peer_f32(uint32_t addr) { return __uint_as_float(ld_peer(addr)); }
+__device__ __forceinline__ float4 ld_peer_v4(uint32_t addr) {  // 16-byte aligned
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+  return v;
+}
 
 // Order-preserving 32-bit key of a score: a larger score has a larger key;
 // -0.0 maps like +0.0 and NaN below every number. The top 11 bits are the
