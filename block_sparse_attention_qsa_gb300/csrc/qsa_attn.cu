@@ -825,21 +825,27 @@ AttnPlan attn_plan(const qsa_dims& d, int num_sms) {
   const int min_tiles = d.kv_dtype == QSA_KV_FP8_E4M3 ? kMinTilesPerCta<true> : kMinTilesPerCta<false>;
   const long long most = (total + min_tiles - 1) / min_tiles;
   pl.grid = (int)(most < resident ? most : resident);
-  // The cluster form where it gives no CTA more tiles than stream-K's largest
-  // share and its clusters take at most 4/5 of the resident CTA slots: few
-  // units (small batches), each split over up to kMaxCluster CTAs. Its CTAs'
-  // pieces merge through distributed shared memory instead of the workspace
-  // (pl.grid keeps the stream-K count, which the workspace is sized for and
-  // which the launch falls back to). Measured at batch 8 (64 units, clusters
-  // of 7 filling 448 of 456 slots) the cluster form was slower, 41.7 -> 49.7
-  // us per step: clusters must fit inside one GPC, so a nearly full grid
-  // does not place in one wave.
+  // The cluster form, where its merge on chip outweighs stream-K's balance:
+  // each unit split over c <= kMaxCluster CTAs, with no CTA more than twice
+  // the tiles of stream-K's largest share, and the clusters taking at most
+  // 4/5 of the resident CTA slots, or 17/20 when that leaves fewer than 4
+  // CTAs per unit (clusters must fit inside one GPC: large clusters filling
+  // most slots do not place in one wave). Its CTAs' pieces merge through
+  // distributed shared memory instead of the workspace (pl.grid keeps the
+  // stream-K count, which the workspace is sized for and which the launch
+  // falls back to). Measured against stream-K (config 2): batch 1 29.8 ->
+  // 27.3 us, 4 34.7 -> 31.2, 8 41.7 -> 39.4, 12 49.6 -> 47.1, 16 56.1 ->
+  // 53.3, 24 70.6 -> 68.1; batch 32 (one CTA per unit at most) stays
+  // stream-K. Clusters of 7 at batch 8 filling 448 of 456 slots took 49.7
+  // us, of 8 at batch 6 filling 384 took 37.5 against 36.1 with 7.
   pl.cl = 0;
   const long long share = (total + pl.grid - 1) / pl.grid;
-  long long c = std::min<long long>(kMaxCluster, (pl.tiles + min_tiles - 1) / min_tiles);
-  c = std::min<long long>(c, resident * 4 / 5 / std::max(pl.units, 1));
-  c = std::min<long long>(c, pl.tiles);
-  if (c >= 2 && (pl.tiles + c - 1) / c <= share) pl.cl = (int)c;
+  const long long want = std::min<long long>(std::min<long long>(kMaxCluster, pl.tiles),
+                                             (pl.tiles + min_tiles - 1) / min_tiles);
+  const long long units = std::max(pl.units, 1);
+  long long c = std::min<long long>(want, resident * 4 / 5 / units);
+  if (c < 4) c = std::min<long long>(want, resident * 17 / 20 / units);
+  if (c >= 2 && (pl.tiles + c - 1) / c <= 2 * share) pl.cl = (int)c;
   return pl;
 }
 
