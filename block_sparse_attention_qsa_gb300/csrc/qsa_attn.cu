@@ -42,6 +42,14 @@
 // publishes (max, sum, acc) pieces to the workspace and the last piece to
 // arrive, counted by an atomic ticket, merges them and resets the ticket, so
 // there is no spin-wait anywhere.
+//
+// Cluster form (up to mid-size batches, chosen by attn_plan): each unit is
+// one thread-block cluster whose CTAs split its tiles evenly and run the same
+// warp loop; their pieces stay in shared memory and are merged through
+// distributed shared memory between two hardware cluster barriers, with no
+// workspace round trip. Measured on GB300 it beats stream-K's even shares
+// wherever no CTA gets more than about twice stream-K's tiles and the
+// clusters still place in one wave.
 #include <algorithm>
 
 #include "qsa_internal.cuh"
