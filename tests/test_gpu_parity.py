@@ -516,6 +516,16 @@ def test_decode_full_size_batch32_every_row(qsa, config):
     assert n == 128 and skipped <= 2
 
 
+@pytest.mark.parametrize("config,batch", [(2, 8), (2, 16), (2, 24), (3, 8)])
+def test_decode_full_size_every_row_mid_batches(qsa, config, batch):
+    # batches whose attention runs in the cluster form with 5, 3 and 2 CTAs per
+    # unit (units of the verify batch split over one thread-block cluster each),
+    # every row checked stage by stage like batch 32
+    spec = synth.spec_for(config, batch=batch)
+    skipped, n = _decode_and_compare(qsa, spec)
+    assert n == 4 * batch and skipped <= 2
+
+
 def test_decode_long_context_batch1_sampled(qsa):
     spec = synth.spec_for(4, batch=1, ctx=131072)
     skipped, n = _decode_and_compare(qsa, spec, rows=[(0, 0), (0, 3)])
