@@ -45,9 +45,10 @@
 //
 // Cluster form (up to mid-size batches, chosen by attn_plan): each unit is
 // one thread-block cluster whose CTAs split its tiles evenly and run the same
-// warp loop; their pieces stay in shared memory and are merged through
-// distributed shared memory between two hardware cluster barriers, with no
-// workspace round trip. Measured on GB300 it beats stream-K's even shares
+// warp loop; each CTA then stores its piece's values of every other CTA's
+// share of the outputs into that CTA's shared memory (distributed shared
+// memory), and after one hardware cluster barrier every CTA merges its share
+// locally, with no workspace round trip. Measured on GB300 it beats stream-K's even shares
 // wherever no CTA gets more than about twice stream-K's tiles and the
 // clusters still place in one wave.
 #include <algorithm>
@@ -76,6 +77,14 @@ template <bool FP8>
 constexpr int kMinTilesPerCta = FP8 ? 2 : 3;
 constexpr int kMergeBatch = 4;  // pieces whose accumulators are read at once
 constexpr int kMaxCluster = 16;  // CTAs per unit in the cluster form (non-portable above 8)
+// inbox of the cluster form: C sources x (4 ceil(256 / C)) outputs; checked
+// below to cover every C in 2..kMaxCluster (at most 15 x 72 = 1,080 floats),
+// a multiple of 4 (float4 reads)
+constexpr int kInboxAcc = 1088;
+constexpr bool inbox_fits(int c) {
+  return c > kMaxCluster || (c * 4 * ((256 + c - 1) / c) <= kInboxAcc && inbox_fits(c + 1));
+}
+static_assert(inbox_fits(2) && kInboxAcc % 4 == 0, "cluster-form inbox too small");
 constexpr int kThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -246,15 +255,17 @@ struct Cursor {
 
 // CL: the cluster form for few units. Each unit is one thread-block cluster
 // of a.cl CTAs, CTA k taking the unit's tiles [k T / cl, (k+1) T / cl); the
-// CTAs' pieces stay in their shared memory and are merged through
-// distributed shared memory between two cluster barriers (each CTA merges
-// 1 / cl of the unit's outputs), with no workspace, fence or ticket.
+// CTAs' pieces are pushed through distributed shared memory to the CTAs that
+// own each 1 / cl of the unit's outputs and merged there after one cluster
+// barrier, with no workspace, fence or ticket.
 template <bool FP8, bool CL>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const AttnArgs a) {
   __shared__ __align__(16) __nv_bfloat16 sQ[2][kGroup * kDim];
   __shared__ __align__(16) float wacc[4 * kGroup * kDim];  // [warp][head][dim]
   __shared__ float s_ml[96];
   __shared__ int s_last;
+  // cluster form: the other CTAs' values of this CTA's outputs (its inbox)
+  __shared__ __align__(16) float inbox[CL ? kInboxAcc + 16 * kMaxCluster : 4];
 
   // positions per warp step: lane 4g + c holds rows g + 8k, k < R, so each
   // pair of rows fills the 16 M rows of a score mma and the k of a PV mma.
@@ -587,43 +598,42 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
         orow[h * kDim + tid] = __float2bfloat16_rn(l > 0.f ? o[h] / l * vscale : 0.f);
       }
     } else if constexpr (CL) {
-      // ---- the cluster's pieces: this CTA's (sM, sL) and accumulators stay in
-      // its shared memory; after the barrier each CTA merges its share of the
-      // unit's 8 x 128 outputs from every CTA's piece ----
-      float* pacc = wacc;  // [8][128] (free once every thread has summed its o[])
-      __syncthreads();
-#pragma unroll
-      for (int h = 0; h < 8; ++h) pacc[h * kDim + tid] = o[h];
-      cluster_sync();
+      // ---- the cluster's pieces: CTA k owns quads [k per, (k+1) per) of the
+      // unit's 256 four-dim output quads. Every CTA stores its piece's values
+      // for each owner's outputs, and its (max, sum), straight into that
+      // owner's inbox (distributed shared memory stores, in flight while the
+      // CTAs wait at the barrier); after the one barrier each owner merges
+      // from its own shared memory, and no CTA touches another's again ----
       const int C = a.cl, rk = (int)cluster_rank();
-      // every piece's (max, sum) once, into this CTA's [C][16] table (beside
-      // pacc: no peer reads it)
-      float* pml = wacc + kGroup * kDim;
-      for (int i = tid; i < 16 * C; i += kThreads) {
-        const int j = i >> 4, e = i & 15;
-        pml[i] = ld_peer_f32(peer_addr(e < 8 ? sM + e : sL + (e - 8), j));
-      }
-      __syncthreads();
-      // this CTA's outputs, four consecutive dims of one head per thread
       constexpr int kQuads = kGroup * kDim / 4;
-      const int per = (kQuads + C - 1) / C, q_end = min(kQuads, (rk + 1) * per);
+      const int per = (kQuads + C - 1) / C, span = 4 * per;  // outputs per owner
+      float* in_acc = inbox;               // [C][span]: the sources' accumulators of this CTA's outputs
+      float* in_ml = inbox + kInboxAcc;    // [C][16]: the sources' (max[8], sum[8])
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        const int oi = h * kDim + tid, r = oi / span;
+        st_peer_f32(peer_addr(in_acc + rk * span + (oi - r * span), r), o[h]);
+      }
+      for (int i = tid; i < 16 * C; i += kThreads) {
+        const int r = i >> 4, e = i & 15;
+        st_peer_f32(peer_addr(in_ml + rk * 16 + e, r), e < 8 ? sM[e] : sL[e - 8]);
+      }
+      cluster_sync();  // release / acquire: every store above is visible to its owner
+      const int q_end = min(kQuads, (rk + 1) * per);
       for (int qd = rk * per + tid; qd < q_end; qd += kThreads) {
-        const int oi = 4 * qd, h = oi / kDim;
+        const int oi = 4 * qd, h = oi / kDim, li = oi - rk * span;
         float M = kNegInf;
-        for (int j = 0; j < C; ++j) M = fmaxf(M, pml[16 * j + h]);
+        for (int j = 0; j < C; ++j) M = fmaxf(M, in_ml[16 * j + h]);
         const float Mb = M == kNegInf ? 0.f : M;
         float L = 0.f, O0 = 0.f, O1 = 0.f, O2 = 0.f, O3 = 0.f;
-#pragma unroll
-        for (int j = 0; j < kMaxCluster; ++j) {
-          if (j < C) {
-            const float4 x = ld_peer_v4(peer_addr(pacc + oi, j));
-            const float f = exp2f(pml[16 * j + h] - Mb);
-            L += pml[16 * j + 8 + h] * f;
-            O0 += x.x * f;
-            O1 += x.y * f;
-            O2 += x.z * f;
-            O3 += x.w * f;
-          }
+        for (int j = 0; j < C; ++j) {
+          const float4 x = *reinterpret_cast<const float4*>(in_acc + j * span + li);
+          const float f = exp2f(in_ml[16 * j + h] - Mb);
+          L += in_ml[16 * j + 8 + h] * f;
+          O0 += x.x * f;
+          O1 += x.y * f;
+          O2 += x.z * f;
+          O3 += x.w * f;
         }
         const float sc = L > 0.f ? vscale / L : 0.f;
         __nv_bfloat16* dst = orow + oi;  // dims oi .. oi + 3 of head h
@@ -641,7 +651,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
         }
       }
       QSA_MARK(6);
-      cluster_sync();  // no CTA leaves while another may still read its piece
     } else {
       // ---- a piece of the unit: publish it, the last piece to arrive merges ----
       // slot 2c: the share's first segment, 2c + 1: its last (only these two can be pieces)

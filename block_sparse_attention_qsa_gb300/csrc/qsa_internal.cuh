@@ -118,7 +118,7 @@ __device__ __forceinline__ void record_error(int32_t* hdr, int32_t kind, int32_t
 __device__ __forceinline__ int n_full_of(int p) { return (p + 1) >> 2; }
 
 // thread-block clusters: rank, size, the hardware barrier (release / acquire),
-// and loads from another CTA's shared memory (distributed shared memory)
+// and loads from / stores to another CTA's shared memory (distributed shared memory)
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -143,11 +143,8 @@ __device__ __forceinline__ uint32_t ld_peer(uint32_t addr) {
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
-__device__ __forceinline__ float ld_peer_f32(uint32_t addr) { return __uint_as_float(ld_peer(addr)); }
-__device__ __forceinline__ float4 ld_peer_v4(uint32_t addr) {  // 16-byte aligned
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
-  return v;
+__device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 // Order-preserving 32-bit key of a score: a larger score has a larger key;
