@@ -854,11 +854,17 @@ AttnPlan attn_plan(const qsa_dims& d, int num_sms) {
   // 27.3 us, 4 34.7 -> 31.2, 8 41.7 -> 39.4, 12 49.6 -> 47.1, 16 56.1 ->
   // 53.3, 24 70.6 -> 68.1; batch 32 (one CTA per unit at most) stays
   // stream-K. Clusters of 7 at batch 8 filling 448 of 456 slots took 49.7
-  // us, of 8 at batch 6 filling 384 took 37.5 against 36.1 with 7.
+  // us, of 8 at batch 6 filling 384 took 37.5 against 36.1 with 7. Clusters
+  // of 16 at batch 1 (128 CTAs, one per SM): 26.5 -> 24.9 us against 11; at
+  // batch 2 (256 CTAs) 26.6 -> 27.1, so only where each CTA has an SM; with
+  // FP8 (tiles of 128 positions) 16 against 9 was slower (24.6 -> 25.1 us).
   pl.cl = 0;
   const long long share = (total + pl.grid - 1) / pl.grid;
-  const long long want = std::min<long long>(std::min<long long>(kMaxCluster, pl.tiles),
-                                             (pl.tiles + min_tiles - 1) / min_tiles);
+  // BF16: as many CTAs per unit as keep each on an SM of its own (more CTAs,
+  // shorter loops); otherwise no fewer than min_tiles tiles per CTA
+  long long want = std::min<long long>(kMaxCluster, pl.tiles);
+  if (d.kv_dtype == QSA_KV_FP8_E4M3 || (long long)pl.units * want > num_sms)
+    want = std::min<long long>(want, (pl.tiles + min_tiles - 1) / min_tiles);
   const long long units = std::max(pl.units, 1);
   long long c = std::min<long long>(want, resident * 4 / 5 / units);
   if (c < 4) c = std::min<long long>(want, resident * 17 / 20 / units);
