@@ -287,6 +287,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
   QSA_MARK(0);
   long long w0, w1;
   if constexpr (CL) {
+    // every CTA of the cluster must have started before another stores into
+    // its shared memory: arrive now, wait before the pushes below
+    cluster_arrive_relaxed();
     // one unit per cluster (the host keeps cl <= tiles, so no share is empty)
     const int uu = cta / a.cl, rk = cta - uu * a.cl;
     w0 = (long long)uu * a.tiles + (long long)rk * a.tiles / a.cl;
@@ -609,6 +612,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm<FP8>) attn_kernel(const A
       const int per = (kQuads + C - 1) / C, span = 4 * per;  // outputs per owner
       float* in_acc = inbox;               // [C][span]: the sources' accumulators of this CTA's outputs
       float* in_ml = inbox + kInboxAcc;    // [C][16]: the sources' (max[8], sum[8])
+      cluster_wait();  // every CTA of the cluster has started
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
         const int oi = h * kDim + tid, r = oi / span;

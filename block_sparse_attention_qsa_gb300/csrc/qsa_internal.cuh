@@ -132,6 +132,13 @@ __device__ __forceinline__ uint32_t cluster_size() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// the two halves of a cluster barrier, for a wait placed long after the arrival
+// (e.g. arrive at the start, wait before the first access to another CTA's
+// shared memory, which must not come before every CTA of the cluster started)
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 // address of `p` (this CTA's shared memory) in CTA `rank` of the cluster
 __device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
   uint32_t a;
