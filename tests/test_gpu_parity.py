@@ -549,11 +549,13 @@ def test_decode_long_context_batch8_cluster_rows_sampled(qsa):
     assert skipped <= 1
 
 
-def test_decode_replayed_as_a_cuda_graph_matches_direct_calls(qsa):
+@pytest.mark.parametrize("batch", [32, 1, 8])
+def test_decode_replayed_as_a_cuda_graph_matches_direct_calls(qsa, batch):
     # the launch the benchmark times: the fused step captured once as a CUDA
     # graph (kernels and programmatic dependencies) and replayed, at full size;
-    # its outputs must equal those of direct calls bit for bit, replay after replay
-    spec = synth.spec_for(2)
+    # its outputs must equal those of direct calls bit for bit, replay after
+    # replay (batch 32: stream-K attention; 1 and 8: its cluster form)
+    spec = synth.spec_for(2, batch=batch)
     g = synth.make_inputs(spec, device="cuda")
     d = qsa.dims_for_spec(spec)
     ws = qsa.make_workspace(d)
