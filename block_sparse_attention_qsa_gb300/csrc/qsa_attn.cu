@@ -68,13 +68,11 @@ template <bool FP8>
 constexpr int kCtasPerSm = 3;
 template <bool FP8>
 constexpr int kRowsPerLane = FP8 ? 4 : 2;
-// Small batches in the stream-K form: each CTA takes at least this many tiles
-// (192 BF16 or 256 FP8 positions), so a unit is cut into few pieces and the
-// merge of the last one to arrive stays short. Measured at batch 1, BF16: 1
-// tile 35.1 us per step, 2 tiles 30.7, 3 tiles 28.9, 4 tiles 33.5 (the first
-// and last with an older build); FP8 (tiles twice as long): 2 tiles 31.0, 3
-// tiles 32.1. The cluster form (whose merge is on chip) uses it as its
-// lower bound where CTAs share SMs.
+// Small batches: each CTA takes at least this many tiles (192 BF16 or 256 FP8
+// positions), so a unit is cut into few pieces and the merge of the last one
+// to arrive stays short. Measured at batch 1, BF16: 1 tile 35.1 us per step,
+// 2 tiles 30.7, 3 tiles 28.9, 4 tiles 33.5 (the first and last with an older
+// build); FP8 (tiles twice as long): 2 tiles 31.0, 3 tiles 32.1.
 template <bool FP8>
 constexpr int kMinTilesPerCta = FP8 ? 2 : 3;
 constexpr int kMergeBatch = 4;  // pieces whose accumulators are read at once
